@@ -1,0 +1,145 @@
+"""CPU oracle for row-wise top-k (RTop-K) and the MaxK layer.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product path
+(``maxk_sparse_activations_gb300``) never imports it, and the two share no code:
+the arithmetic lives in ``rtopk_oracle.c`` (plain C, binary32, no FMA
+contraction), which this module compiles with gcc and calls through ctypes.
+Inputs come from the seeded generators in ``maxk_sparse_activations_gb300.synth``,
+a module that holds none of the method's arithmetic.
+
+Functions (each follows the page and section named in ``rtopk_oracle.c``):
+
+* ``sort_topk(x, k)`` -- the definition of exact top-k: order the row by value
+  descending then index ascending, take the first k, list them by index.
+  ("RTop-K ..." summary, "Problem".)
+* ``brute_topk(x, k)`` -- the same result found by enumerating every k-subset
+  of a tiny row (M <= 20); an independent pin of ``sort_topk``.
+* ``replay(x, k, max_iter, eps)`` -- the method step by step: min/max range,
+  bisection on the binary32 midpoint with ``>=`` counting, ``max_iter`` early
+  stop, ``eps`` stop, and the fill pass of borderline ties by lowest index.
+  ("RTop-K ..." summary, "Approach".)
+* ``maxk_backward(dy, idx, M)`` -- the MaxK backward scatter: the gradient row
+  is zero except at the kept positions. ("MaxK-GNN ...", "How MaxK-GNN works",
+  "Asymmetric passes, one mask".)
+
+bf16 inputs are widened exactly to binary32 (the 16 bits become the top half of
+the word) and run through the same functions; kept values are the original
+16-bit patterns gathered at the kept indices.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rtopk_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, EARG, EINPUT, ENOMEM = 0, -1, -2, -3
+
+
+def build(force: bool = False) -> str:
+    """Compile ``rtopk_oracle.c`` into ``liboracle.so`` (in-tree, git-ignored)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            p, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+            lib.oracle_sort_topk.argtypes = [p, i64, i32, i32, p]
+            lib.oracle_brute_topk.argtypes = [p, i64, i32, i32, p]
+            lib.oracle_replay.argtypes = [p, i64, i32, i32, i32, f32, p, p]
+            lib.oracle_maxk_backward_u16.argtypes = [p, p, i64, i32, i32, p]
+            for f in (lib.oracle_sort_topk, lib.oracle_brute_topk, lib.oracle_replay,
+                      lib.oracle_maxk_backward_u16):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc == EINPUT:
+        raise ValueError(f"{what}: input row is non-finite or has |x| > 1e38")
+    if rc != OK:
+        raise ValueError(f"{what}: invalid arguments (code {rc})")
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """Exact bf16 -> binary32: the 16 bits become the high half of the word."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _as_f32_rows(x: np.ndarray):
+    """Returns (fp32 view used for the arithmetic, original array for values)."""
+    if x.dtype == np.float32:
+        return np.ascontiguousarray(x), np.ascontiguousarray(x)
+    if x.dtype == np.uint16:  # raw bf16 bit patterns
+        return widen_bf16(x), np.ascontiguousarray(x)
+    raise TypeError("oracle inputs are float32 or uint16 (bf16 bit patterns)")
+
+
+def _gather(orig: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    return np.take_along_axis(orig, idx.astype(np.int64), axis=1)
+
+
+def sort_topk(x: np.ndarray, k: int):
+    """Exact top-k by the definition. Returns (values, int32 indices), N x k."""
+    xf, orig = _as_f32_rows(x)
+    N, M = xf.shape
+    idx = np.empty((N, k), dtype=np.int32)
+    _check(_load().oracle_sort_topk(_ptr(xf), N, M, k, _ptr(idx)), "sort_topk")
+    return _gather(orig, idx), idx
+
+
+def brute_topk(x: np.ndarray, k: int):
+    """Exact top-k by enumerating all k-subsets (M <= 20)."""
+    xf, orig = _as_f32_rows(x)
+    N, M = xf.shape
+    idx = np.empty((N, k), dtype=np.int32)
+    _check(_load().oracle_brute_topk(_ptr(xf), N, M, k, _ptr(idx)), "brute_topk")
+    return _gather(orig, idx), idx
+
+
+def replay(x: np.ndarray, k: int, max_iter: int = -1, eps: float = 0.0):
+    """Step-by-step replay of the bisection. Returns (values, idx, iters)."""
+    xf, orig = _as_f32_rows(x)
+    N, M = xf.shape
+    idx = np.empty((N, k), dtype=np.int32)
+    iters = np.empty((N,), dtype=np.int32)
+    rc = _load().oracle_replay(_ptr(xf), N, M, k, int(max_iter), float(np.float32(eps)),
+                               _ptr(idx), _ptr(iters))
+    _check(rc, "replay")
+    return _gather(orig, idx), idx, iters
+
+
+def maxk_backward(dy_bits: np.ndarray, idx: np.ndarray, M: int) -> np.ndarray:
+    """MaxK backward scatter of bf16 bit patterns into a zero N x M row block."""
+    dy = np.ascontiguousarray(dy_bits, dtype=np.uint16)
+    ix = np.ascontiguousarray(idx, dtype=np.int16)
+    N, k = dy.shape
+    grad = np.empty((N, M), dtype=np.uint16)
+    _check(_load().oracle_maxk_backward_u16(_ptr(dy), _ptr(ix), N, M, k, _ptr(grad)),
+           "maxk_backward")
+    return grad
