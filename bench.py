@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the row-wise top-k hot path on GB300.
+
+Metric: rows/s and achieved HBM GB/s for row-wise top-k (RTop-K) at
+N = 2^20 rows, M = 256, k = 32, fp32 i.i.d. N(0, 1) (seed 0 + rank), exact mode
+(max_iter = -1, eps = 0), CBSR output fp32 values + int32 indices.
+
+One step = one rtopk_select over the whole 2^20-row batch (every step of the
+path: range, bisection, fill pass, CBSR store -- one kernel launch). Inputs are
+1.07 GB per rank, larger than the 129 MB L2, so no flush is needed between
+steps. Timing: W untimed warm-up steps, then exactly K steps bracketed by a
+barrier and torch.cuda.synchronize() on both sides, CUDA events on the
+launching stream, max over ranks. Multi-GPU: every rank processes its own
+2^20-row batch with no collective on the data path (weak scaling).
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+The reference arm times the CPU oracle (the plain C replay of the method) on
+the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "rows/s and achieved HBM GB/s (% of peak), row-wise top-k M=256 k=32 N=2^20"
+N_ROWS, M_COLS, K_SEL = 1 << 20, 256, 32
+WORKLOAD = ("rtopk_select exact (max_iter=-1, eps=0), N=2^20 rows x M=256 fp32 i.i.d. N(0,1) "
+            "-> CBSR k=32 fp32 values + int32 indices")
+PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
+
+
+def algorithmic_bytes(N, M, k, s_in, s_val, s_idx):
+    """Bytes the method must move: read the matrix once, write the CBSR arrays once."""
+    return N * M * s_in + N * k * (s_val + s_idx)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "maxk_sparse_activations_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches these sources."""
+    for p in glob.glob(PROFILE_GLOB):
+        kv = {}
+        with open(p) as f:
+            for line in f:
+                if line.startswith("- ") and ":" in line:
+                    key, val = line[2:].split(":", 1)
+                    kv[key.strip()] = val.strip().strip("`")
+        if kv.get("bench_tag") == kernel_tag:
+            if kv.get("source_hash") == src_hash and "traffic_bytes_per_launch" in kv:
+                return int(float(kv["traffic_bytes_per_launch"])), p
+            return None, p
+    return None, None
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.uuid = gpu_uuid
+        self.proc = None
+        self.lines: list[tuple[float, str]] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._pump, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _pump(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside if inside else [r for r in rows if r[0] >= t0 - 0.5][:3]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((float(r[3]) for r in used if r[3].replace(".", "", 1).isdigit()),
+                                   default=None)}
+
+
+def rejected_clocks(c: dict) -> bool:
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(c.get("reasons", [])):
+        return True
+    if c.get("sm_mhz") and c.get("sm_max_mhz") and c["sm_mhz"] < 0.6 * c["sm_max_mhz"] \
+            and not c.get("reasons"):
+        return True
+    return False
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ------------------------------------------------------------------------------------------
+def time_oracle(x: np.ndarray, k: int, threads: int, min_seconds: float, max_reps: int):
+    """Wall time of the oracle replay over x split into `threads` contiguous row blocks."""
+    import concurrent.futures as cf
+    import oracle  # test infrastructure; only the CPU-baseline leg uses it
+    oracle.build()
+    blocks = np.array_split(np.arange(x.shape[0]), threads)
+
+    def work(rows):
+        if rows.size:
+            oracle.replay(x[rows[0]:rows[-1] + 1], k, -1, 0.0)
+
+    best, reps, t_all = None, 0, time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while reps < max_reps and (reps < 1 or time.perf_counter() - t_all < min_seconds):
+            t0 = time.perf_counter()
+            list(ex.map(work, blocks))
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+            reps += 1
+    return best, reps
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return 0
+    from maxk_sparse_activations_gb300 import synth
+    threads = os.cpu_count() or 1
+    # calibrate on 16384 rows, then size the per-step sample so K + W steps take about a minute
+    probe = synth.normal_f32(16384, M_COLS, seed=0)
+    t_probe, _ = time_oracle(probe, K_SEL, threads, 0.0, 1)
+    rate = probe.shape[0] / max(t_probe, 1e-9)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows = int(min(N_ROWS, max(4096, rate * budget)))
+    x = synth.normal_f32(N_ROWS, M_COLS, seed=0)[:rows]
+    for _ in range(args.warmup):
+        time_oracle(x, K_SEL, threads, 0.0, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(x, K_SEL, threads, 0.0, 1)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = rows / dt
+    sample = f"first {rows} of the 2^20 rows per step, oracle replay (exact), {threads} threads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "N": N_ROWS, "M": M_COLS, "k": K_SEL, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------
+# GB300 arm
+# ------------------------------------------------------------------------------------------
+def run_gb300(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+    from maxk_sparse_activations_gb300 import _lib, api, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    lib = _lib.load()
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    x_host = synth.normal_f32(N_ROWS, M_COLS, seed=rank)
+    x = torch.from_numpy(x_host).to(dev)
+    vals = torch.empty((N_ROWS, K_SEL), dtype=torch.float32, device=dev)
+    idx = torch.empty((N_ROWS, K_SEL), dtype=torch.int32, device=dev)
+    sptr = stream.cuda_stream
+
+    def step():
+        rc = lib.rtopk_select(x.data_ptr(), N_ROWS, M_COLS, K_SEL, -1, 0.0, _lib.RTOPK_F32,
+                              vals.data_ptr(), idx.data_ptr(), sptr)
+        if rc != 0:
+            raise RuntimeError(_lib.strerror(rc))
+
+    def timed(fn, steps):
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = None
+    for attempt in range(2):
+        sampler = ClockSampler(uuid) if rank == 0 else None
+        if sampler:
+            sampler.start()
+        w0 = time.time()
+        ms = timed(step, args.steps)
+        w1 = time.time()
+        if sampler:
+            sampler.stop()
+            clocks = sampler.summary(w0, w1)
+        redo = torch.tensor([1 if (clocks and rejected_clocks(clocks)) else 0], device=dev)
+        if world > 1:
+            dist.broadcast(redo, 0)
+        if not int(redo.item()) or attempt == 1:
+            break
+    ms_per_step = ms / args.steps
+    rows_per_s = world * N_ROWS / (ms_per_step * 1e-3)
+    bytes_step = algorithmic_bytes(N_ROWS, M_COLS, K_SEL, 4, 4, 4)
+    gbs = bytes_step / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    src_hash = kernel_source_hash()
+    traffic, prof = profiled_traffic("rtopk_select_f32_M256_k32", src_hash)
+
+    # ---- end to end through the public API: pinned host -> device -> select -> host
+    x_pin = torch.from_numpy(x_host).pin_memory()
+    v_pin = torch.empty((N_ROWS, K_SEL), dtype=torch.float32).pin_memory()
+    i_pin = torch.empty((N_ROWS, K_SEL), dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        x.copy_(x_pin, non_blocking=True)
+        api.rtopk_select(x, K_SEL, vals=vals, idx=idx)
+        v_pin.copy_(vals, non_blocking=True)
+        i_pin.copy_(idx, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    ms_e2e = timed(e2e_step, e2e_steps) / e2e_steps
+
+    extra = {}
+    if not args.no_extra:
+        extra = secondary_measurements(torch, api, synth, dev, x, stream, world, timed)
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            threads = os.cpu_count() or 1
+            t_cpu, reps = time_oracle(x_host, K_SEL, threads, 5.0, 3)
+            cpu = {"value": N_ROWS / t_cpu, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                   "sample": f"all 2^20 rows of the workload, oracle replay (exact), best of {reps}, "
+                             f"{threads} threads on contiguous row blocks"}
+        line = {
+            "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "N": N_ROWS, "M": M_COLS, "k": K_SEL, "max_iter": -1,
+                       "eps": 0.0, "l2": "inputs larger than L2 (1.07 GB per rank; L2 129 MB)",
+                       "parallelism": f"rows: one 2^20-row batch per rank x {world}"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
+                         else "fallback", "algorithmic_bytes_per_launch": bytes_step,
+                         "kernel": "rtopk_select_kernel<float,G=2,W=1,FULL>",
+                         "traffic_source": os.path.relpath(prof, ROOT) if prof else None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * N_ROWS / (ms_e2e * 1e-3), "unit": "rows/s",
+                    "h2d_bytes_per_step": N_ROWS * M_COLS * 4, "d2h_bytes_per_step": N_ROWS * K_SEL * 8,
+                    "ms_per_step": ms_e2e},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "hbm_gbs": gbs, "pct_of_nominal_8tbs": gbs / 8000.0,
+            "source_hash": src_hash,
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
+    """Early-stop speed, the pass-count histogram, and the fused MaxK layer (bf16)."""
+    out = {}
+    N, M, k = N_ROWS, M_COLS, K_SEL
+    vals = torch.empty((N, k), dtype=torch.float32, device=dev)
+    idx = torch.empty((N, k), dtype=torch.int32, device=dev)
+    reps = 50
+    for m in (-1, 2, 5):
+        f = lambda: api.rtopk_select(x, k, m, 0.0, vals=vals, idx=idx)
+        f()
+        out[f"rtopk_f32_max_iter_{m}_us"] = timed(f, reps) / reps * 1e3
+    _, _, iters, st = api.rtopk_select_stats(x, k)
+    it = iters.cpu().numpy()
+    out["passes_exact"] = {"median": float(np.median(it)), "p90": float(np.percentile(it, 90)),
+                           "max": int(it.max()), "frac_le_16": float(np.mean(it <= 16)),
+                           "status": int(st.item())}
+    xb = torch.from_numpy(synth.normal_bf16(N, M, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    fv = torch.empty((N, k), dtype=torch.bfloat16, device=dev)
+    fi = torch.empty((N, k), dtype=torch.int16, device=dev)
+    fwd = lambda: api.maxk_forward(xb, k, vals=fv, idx=fi)
+    fwd()
+    t_f = timed(fwd, reps) / reps
+    dy = torch.from_numpy(synth.normal_bf16(N, k, seed=1).view(np.int16)).view(torch.bfloat16).to(dev)
+    g = torch.empty((N, M), dtype=torch.bfloat16, device=dev)
+    bwd = lambda: api.maxk_backward_scatter(dy, fi, M, grad=g)
+    bwd()
+    t_b = timed(bwd, reps) / reps
+    bytes_f = algorithmic_bytes(N, M, k, 2, 2, 2)
+    bytes_b = N * k * 4 + N * M * 2
+    out["maxk_forward_bf16"] = {"us": t_f * 1e3, "gbs": bytes_f / (t_f * 1e-3) / 1e9,
+                                "rows_per_s": N / (t_f * 1e-3), "bytes": bytes_f}
+    out["maxk_backward_scatter_bf16"] = {"us": t_b * 1e3, "gbs": bytes_b / (t_b * 1e-3) / 1e9,
+                                         "bytes": bytes_b}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=N_ROWS,
+                    help="rows per rank (default 2^20, the metric's workload; smaller only for profiling)")
+    args = ap.parse_args()
+    global N_ROWS
+    N_ROWS = args.rows
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "gb300":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_gb300(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

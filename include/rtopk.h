@@ -1,0 +1,153 @@
+/*
+ * rtopk.h -- C ABI of librtopk.so: row-wise top-k selection (RTop-K) and the
+ * MaxK sparse-activation layer on NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page titles and sections):
+ *  [RTopK] "RTop-K: Ultra-Fast Row-Wise Top-K Selection for Neural Network
+ *          Acceleration on GPUs" (summary page): "Problem" (row-wise top-k of
+ *          a large batch of short vectors, output need not be sorted),
+ *          "Approach" (binary search over the value range for a threshold
+ *          selecting k, early stop by capping iterations, second pass filling
+ *          borderline ties), "Surprising findings" (precision epsilon),
+ *          "Limitations" (M > 8192 unsupported).
+ *  [MaxK]  "MaxK-GNN: Extremely Fast GPU Kernel Design for Accelerating Graph
+ *          Neural Networks Training": "How MaxK-GNN works" ("The idea": exactly
+ *          k survivors per row stored as two dense arrays; "Asymmetric passes,
+ *          one mask": the forward sp_index is reused by the backward pass),
+ *          "Why it works".
+ *
+ * Conventions shared by every entry point:
+ *  - All array pointers are caller-owned DEVICE memory (e.g. torch tensors),
+ *    dense and row-major: inputs have row stride M, CBSR outputs row stride k.
+ *    The library allocates no memory and keeps no state between calls, except
+ *    a per-device cache of the SM count and occupancy used to size grids.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream).
+ *  - Argument errors return a negative code synchronously and launch nothing.
+ *    A failed launch returns RTOPK_ECUDA. Problems found in the data on the
+ *    device are reported through the optional `status` word (see below).
+ *  - N == 0 is a no-op that returns RTOPK_OK.
+ *  - Input values must be finite with |x| <= 1e38, so that the binary32
+ *    midpoint (lo + hi) * 0.5 cannot overflow. Rows that break this set a
+ *    status bit; their outputs are unspecified but every write stays inside
+ *    the row.
+ *
+ * Semantics of the selection (identical for every entry point that selects):
+ *  lo = min(row), hi = max(row), c(t) = #{j : x_j >= t}.
+ *  1. If c(hi) >= k: keep the k lowest indices whose value equals the maximum;
+ *     no search pass runs (iters = 0).
+ *  2. Otherwise repeat while (max_iter < 0 or iters < max_iter) and
+ *     (hi - lo) > eps:  mid = (lo + hi) * 0.5 (binary32, no FMA); stop if no
+ *     binary32 value lies strictly between lo and hi; cnt = c(mid); iters++;
+ *     cnt == k: lo = mid and stop; cnt > k: lo = mid; cnt < k: hi = mid.
+ *  3. Keep every x >= hi, then fill up to exactly k from lo <= x < hi in
+ *     ascending index order.
+ *  4. Write the k kept (value, index) pairs of the row in ascending index
+ *     order; values are bit copies of the input.
+ *  With max_iter < 0 and eps == 0 (exact mode) the result is the exact top-k
+ *  with ties at the k-th value broken by the lowest index.
+ *
+ * Device status word bits (OR-ed with atomicOr; the caller zeroes the word
+ * before the call and reads it after synchronising the stream):
+ */
+#ifndef RTOPK_H_
+#define RTOPK_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RTOPK_STATUS_NONFINITE  0x1u /* a row holds NaN or +-Inf */
+#define RTOPK_STATUS_RANGE      0x2u /* a row holds a finite value with |x| > 1e38 */
+#define RTOPK_STATUS_SAFETY_CAP 0x4u /* a search reached 512 passes (cannot happen for valid rows) */
+#define RTOPK_STATUS_BAD_INDEX  0x8u /* backward: an index outside [0, M) was skipped */
+
+#define RTOPK_MAX_M 8192 /* [RTopK] "Limitations": rows longer than 8192 are unsupported */
+
+typedef enum {
+  RTOPK_F32 = 0,  /* IEEE binary32 */
+  RTOPK_BF16 = 1  /* bfloat16, passed as 16-bit patterns */
+} rtopk_dtype;
+
+typedef enum {
+  RTOPK_OK = 0,
+  RTOPK_EINVAL_SHAPE = -1, /* N < 0, M < 1 or M > RTOPK_MAX_M */
+  RTOPK_EINVAL_K = -2,     /* k < 1 or k > M */
+  RTOPK_EINVAL_PTR = -3,   /* a required pointer is NULL (with N > 0) */
+  RTOPK_EINVAL_DTYPE = -4, /* dtype is not an rtopk_dtype value */
+  RTOPK_ECUDA = -5,        /* a CUDA runtime call or launch failed */
+  RTOPK_EINVAL_ARG = -6    /* eps < 0 or NaN */
+} rtopk_status;
+
+/*
+ * rtopk_select -- row-wise top-k of an N x M matrix into CBSR.
+ * [RTopK] "Problem", "Approach"; [MaxK] "The idea" (CBSR = two dense N x k arrays).
+ *
+ *  in        device, N x M, dtype elements (fp32 or bf16 bit patterns), read only
+ *  N, M, k   rows, row length (1..8192), kept per row (1..M)
+ *  max_iter  cap on counted bisection passes; < 0 = no cap (early stop off)
+ *  eps       absolute precision: the search stops once (hi - lo) <= eps; >= 0
+ *  dtype     RTOPK_F32 or RTOPK_BF16
+ *  vals      device, N x k, same dtype as `in`: the kept values (bit copies)
+ *  idx       device, N x k int32: the kept column indices, ascending per row
+ *  stream    CUDA stream to launch on
+ * Returns RTOPK_OK or a negative rtopk_status.
+ */
+int rtopk_select(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_iter, float eps,
+                 int32_t dtype, void* vals, int32_t* idx, cudaStream_t stream);
+
+/*
+ * rtopk_select_stats -- rtopk_select plus diagnostics (same kernel, same outputs).
+ * [RTopK] "Surprising findings" (exact selection exits within 16 iterations in
+ * most cases) -- `iters` measures exactly that per row.
+ *
+ *  iters   device, N int32 or NULL: counted bisection passes of each row
+ *  status  device, one uint32 or NULL: OR of RTOPK_STATUS_* bits over all rows
+ */
+int rtopk_select_stats(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_iter,
+                       float eps, int32_t dtype, void* vals, int32_t* idx, int32_t* iters,
+                       uint32_t* status, cudaStream_t stream);
+
+/*
+ * maxk_forward -- the MaxK nonlinearity: keep the top-k features of each row of
+ * a bf16 activation matrix, written as CBSR with 16-bit indices.
+ * [MaxK] "The idea" (exactly k survivors per node, dense data + sp_index arrays).
+ *
+ *  in_bf16    device, N x M bf16 bit patterns
+ *  vals_bf16  device, N x k bf16: sp_data
+ *  idx        device, N x k int16: sp_index, ascending per row (M <= 8192 < 2^15)
+ *  other arguments as for rtopk_select; exact mode by default (max_iter = -1, eps = 0)
+ */
+int maxk_forward(const void* in_bf16, int64_t N, int32_t M, int32_t k, int32_t max_iter,
+                 float eps, void* vals_bf16, int16_t* idx, cudaStream_t stream);
+
+/*
+ * maxk_backward_scatter -- MaxK backward: gradient flows only to the kept
+ * features, at the positions the forward pass recorded.
+ * [MaxK] "Asymmetric passes, one mask"; "Why it works" (only MaxK survivors
+ * carry gradients).
+ *
+ *  dy_bf16    device, N x k bf16: upstream gradient w.r.t. the CBSR values
+ *  idx        device, N x k int16: the forward sp_index (distinct per row)
+ *  grad_bf16  device, N x M bf16: written in full -- dy at the kept positions,
+ *             +0.0 everywhere else (no separate zero-fill is needed)
+ *  status     device uint32 or NULL: RTOPK_STATUS_BAD_INDEX if an index was
+ *             outside [0, M) (that entry is skipped)
+ * Indices repeated within a row leave which of their values lands unspecified.
+ */
+int maxk_backward_scatter(const void* dy_bf16, const int16_t* idx, int64_t N, int32_t M,
+                          int32_t k, void* grad_bf16, uint32_t* status, cudaStream_t stream);
+
+/* Human-readable text for an rtopk_status code (static storage, never NULL). */
+const char* rtopk_strerror(int code);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int rtopk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RTOPK_H_ */

@@ -1,0 +1,133 @@
+"""Python binding of the C ABI (argument marshalling only).
+
+Every function here checks shapes and dtypes, allocates outputs with torch when
+the caller passes none, and calls the same-named entry point of librtopk.so on
+the current CUDA stream. All selection and scatter work runs in the library's
+CUDA kernels; nothing here computes on the host.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _need_cuda_2d(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def rtopk_select(x: torch.Tensor, k: int, max_iter: int = -1, eps: float = 0.0, *,
+                 vals: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
+    """Row-wise top-k of x (N x M, fp32 or bf16) -> (vals N x k, idx N x k int32)."""
+    vals, idx, _, _ = rtopk_select_stats(x, k, max_iter, eps, vals=vals, idx=idx, stats=False,
+                                         stream=stream)
+    return vals, idx
+
+
+def rtopk_select_stats(x: torch.Tensor, k: int, max_iter: int = -1, eps: float = 0.0, *,
+                       vals: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                       iters: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                       stats: bool = True, stream: Optional[torch.cuda.Stream] = None):
+    """rtopk_select plus per-row pass counts and the device status word.
+
+    Returns (vals, idx, iters, status); iters is int32 of length N and status a
+    one-element int32 tensor holding the OR of the STATUS_* bits (zeroed here
+    before the launch when this function allocates it).
+    """
+    _need_cuda_2d(x, "x")
+    if x.dtype == torch.float32:
+        dtype = _lib.RTOPK_F32
+    elif x.dtype == torch.bfloat16:
+        dtype = _lib.RTOPK_BF16
+    else:
+        raise ValueError("x must be float32 or bfloat16")
+    N, M = x.shape
+    if vals is None:
+        vals = torch.empty((N, k), dtype=x.dtype, device=x.device)
+    if idx is None:
+        idx = torch.empty((N, k), dtype=torch.int32, device=x.device)
+    if stats:
+        if iters is None:
+            iters = torch.empty((N,), dtype=torch.int32, device=x.device)
+        if status is None:
+            status = torch.zeros((1,), dtype=torch.int32, device=x.device)
+    lib = _lib.load()
+    if stats:
+        rc = lib.rtopk_select_stats(x.data_ptr(), N, M, int(k), int(max_iter), float(eps), dtype,
+                                    vals.data_ptr(), idx.data_ptr(), _ptr(iters), _ptr(status),
+                                    _stream_ptr(stream, x.device))
+    else:
+        rc = lib.rtopk_select(x.data_ptr(), N, M, int(k), int(max_iter), float(eps), dtype,
+                              vals.data_ptr(), idx.data_ptr(), _stream_ptr(stream, x.device))
+    _lib.check(rc, "rtopk_select")
+    return vals, idx, iters, status
+
+
+def maxk_forward(x: torch.Tensor, k: int, max_iter: int = -1, eps: float = 0.0, *,
+                 vals: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
+    """MaxK nonlinearity: bf16 x (N x M) -> CBSR (sp_data bf16 N x k, sp_index int16 N x k)."""
+    _need_cuda_2d(x, "x")
+    if x.dtype != torch.bfloat16:
+        raise ValueError("maxk_forward takes bfloat16 input")
+    N, M = x.shape
+    if vals is None:
+        vals = torch.empty((N, k), dtype=torch.bfloat16, device=x.device)
+    if idx is None:
+        idx = torch.empty((N, k), dtype=torch.int16, device=x.device)
+    rc = _lib.load().maxk_forward(x.data_ptr(), N, M, int(k), int(max_iter), float(eps),
+                                  vals.data_ptr(), idx.data_ptr(), _stream_ptr(stream, x.device))
+    _lib.check(rc, "maxk_forward")
+    return vals, idx
+
+
+def maxk_backward_scatter(dy: torch.Tensor, idx: torch.Tensor, M: int, *,
+                          grad: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """MaxK backward: dense N x M bf16 gradient, dy at idx and zero elsewhere."""
+    _need_cuda_2d(dy, "dy")
+    _need_cuda_2d(idx, "idx")
+    if dy.dtype != torch.bfloat16 or idx.dtype != torch.int16:
+        raise ValueError("dy must be bfloat16 and idx int16")
+    if dy.shape != idx.shape:
+        raise ValueError("dy and idx must have the same N x k shape")
+    N, k = dy.shape
+    if grad is None:
+        grad = torch.empty((N, M), dtype=torch.bfloat16, device=dy.device)
+    rc = _lib.load().maxk_backward_scatter(dy.data_ptr(), idx.data_ptr(), N, int(M), int(k),
+                                           grad.data_ptr(), _ptr(status), _stream_ptr(stream, dy.device))
+    _lib.check(rc, "maxk_backward_scatter")
+    return grad
+
+
+class MaxK(torch.autograd.Function):
+    """Autograd wrapper: forward keeps the top-k of each row (CBSR), backward
+    scatters the gradient of the kept values back to their recorded positions."""
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, k: int):
+        vals, idx = maxk_forward(x.contiguous(), k)
+        ctx.save_for_backward(idx)
+        ctx.M = x.shape[1]
+        ctx.mark_non_differentiable(idx)
+        return vals, idx
+
+    @staticmethod
+    def backward(ctx, dvals: torch.Tensor, _didx):
+        (idx,) = ctx.saved_tensors
+        return maxk_backward_scatter(dvals.contiguous(), idx, ctx.M), None

@@ -1,0 +1,48 @@
+// Grid sizing for the persistent kernels: one cache entry per (device, kernel).
+#include <mutex>
+
+#include "launch.h"
+
+namespace rtopk {
+namespace {
+
+struct Entry {
+  int device;
+  const void* kernel;
+  int threads;
+  int blocks;
+};
+constexpr int kMaxEntries = 256;
+Entry g_cache[kMaxEntries];
+int g_used = 0;
+std::mutex g_mu;
+
+}  // namespace
+
+int persistent_blocks(const void* kernel, int threads, size_t smem, int64_t blocks_needed) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int per_gpu = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < g_used; ++i) {
+      if (g_cache[i].device == dev && g_cache[i].kernel == kernel && g_cache[i].threads == threads) {
+        per_gpu = g_cache[i].blocks;
+        break;
+      }
+    }
+  }
+  if (per_gpu == 0) {
+    int sms = 0, occ = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess)
+      return 0;
+    per_gpu = sms * (occ > 0 ? occ : 1);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_used < kMaxEntries) g_cache[g_used++] = Entry{dev, kernel, threads, per_gpu};
+  }
+  if (blocks_needed < 1) blocks_needed = 1;
+  return int(blocks_needed < per_gpu ? blocks_needed : per_gpu);
+}
+
+}  // namespace rtopk

@@ -1,0 +1,64 @@
+"""The C ABI without a GPU: the library builds, exports every symbol that
+include/rtopk.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "rtopk.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from maxk_sparse_activations_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    from maxk_sparse_activations_gb300 import _lib
+    assert set(_lib.EXPORTED) <= set(names)
+    assert {"rtopk_select", "rtopk_select_stats", "maxk_forward", "maxk_backward_scatter"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_version(lib):
+    from maxk_sparse_activations_gb300 import _lib
+    assert _lib.strerror(0) == "ok"
+    default = _lib.strerror(-99)
+    assert "unknown rtopk status" in default
+    texts = {_lib.strerror(code) for code in (-1, -2, -3, -4, -5, -6)}
+    assert len(texts) == 6 and default not in texts
+    assert lib.rtopk_version() >= 100
+
+
+def test_argument_errors_launch_nothing(lib):
+    # every call below must return before any CUDA call (no GPU here)
+    S = lambda *a: lib.rtopk_select(*a)
+    assert S(None, 10, 0, 1, -1, 0.0, 0, None, None, None) == -1          # M < 1
+    assert S(None, 10, 8193, 1, -1, 0.0, 0, None, None, None) == -1       # M > 8192
+    assert S(None, -1, 8, 1, -1, 0.0, 0, None, None, None) == -1          # N < 0
+    assert S(None, 10, 8, 0, -1, 0.0, 0, None, None, None) == -2          # k < 1
+    assert S(None, 10, 8, 9, -1, 0.0, 0, None, None, None) == -2          # k > M
+    assert S(None, 10, 8, 2, -1, 0.0, 0, None, None, None) == -3          # NULL pointers
+    assert S(None, 10, 8, 2, -1, 0.0, 7, None, None, None) == -4          # dtype
+    assert S(None, 10, 8, 2, -1, -1.0, 0, None, None, None) == -6         # eps < 0
+    assert S(None, 10, 8, 2, -1, float("nan"), 0, None, None, None) == -6 # eps NaN
+    assert S(None, 0, 8, 2, -1, 0.0, 0, None, None, None) == 0            # N == 0: no-op
+    assert lib.maxk_forward(None, 5, 8, 9, -1, 0.0, None, None, None) == -2
+    assert lib.maxk_forward(None, 0, 8, 2, -1, 0.0, None, None, None) == 0
+    assert lib.maxk_backward_scatter(None, None, 5, 8, 2, None, None, None) == -3
+    assert lib.maxk_backward_scatter(None, None, 5, 9000, 2, None, None, None) == -1
+    assert lib.maxk_backward_scatter(None, None, 0, 8, 2, None, None, None) == 0

@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA path (through the C ABI binding) against the CPU oracle.
+
+Bar: bit-exact values (raw bits) and indices, and identical per-row pass counts,
+in exact mode and in every early-stop / eps mode (the oracle replays the same
+binary32 search). Workloads follow the five configurations of the method's
+evaluation shape: M = 256, k = 32 normal rows; the MaxK-shaped early-stop study;
+the shape sweep; long rows with adversarial values; the fused MaxK layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from maxk_sparse_activations_gb300 import accuracy, api, synth
+
+from gpu_util import assert_same_selection, to_dev, vals_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    oracle.build()
+
+
+def _run(x, k, max_iter=-1, eps=0.0):
+    xt = to_dev(x)
+    v, i, it, st = api.rtopk_select_stats(xt, k, max_iter, eps)
+    torch.cuda.synchronize()
+    return v, i, it.cpu().numpy(), int(st.item())
+
+
+def _check_full(x, k, max_iter=-1, eps=0.0, what=""):
+    v, i, it, st = _run(x, k, max_iter, eps)
+    ov, oi, oit = oracle.replay(x, k, max_iter, eps)
+    assert st == 0, f"{what}: status {st:#x}"
+    assert_same_selection(v, i, ov, oi, what=what)
+    np.testing.assert_array_equal(it, oit, err_msg=f"{what}: pass counts differ")
+    return v, i, ov, oi
+
+
+def _sample_rows(N, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([np.arange(min(N, 64)), np.arange(max(0, N - 64), N),
+                                     rng.integers(0, N, size=n)]))
+    return rows
+
+
+# ---- configuration 1: exact, N=4096, M=256, k=32, fp32 N(0,1) seed 0 ---------------------
+def test_config1_exact_bit_identical():
+    x = synth.normal_f32(4096, 256, seed=0)
+    v, i, ov, oi = _check_full(x, 32, what="config1")
+    _, si = oracle.sort_topk(x, 32)
+    np.testing.assert_array_equal(i.cpu().numpy(), si)
+
+
+# ---- configuration 2: MaxK-shaped, N=262144, exact and max_iter in {2,3,4,5,8} ------------
+def test_config2_exact_and_early_stop():
+    x = synth.normal_f32(262144, 256, seed=0)
+    _, ie, ove, oie = _check_full(x, 32, what="config2 exact")
+    for m in (2, 3, 4, 5, 8):
+        v, i, _, _ = _check_full(x, 32, max_iter=m, what=f"config2 max_iter={m}")
+        acc = accuracy.compare(vals_np(v).view(np.float32), i.cpu().numpy(), ove, oie)
+        assert acc["r_max_worst"] == 0.0
+        print(f"max_iter={m}: {acc}")
+
+
+# ---- configuration 3: shape sweep (reduced N, every combination) -----------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M", [128, 256, 512, 1024])
+def test_config3_sweep_reduced(M, dtype):
+    x = synth.make("normal", 2048, M, seed=0, dtype=dtype)
+    for k in (16, 32, 64, 128, 256):
+        if k >= M:
+            continue
+        for eps in (0.0, 1e-4, 1e-2):
+            for m in (-1, 2):
+                _check_full(x, k, m, eps, what=f"sweep M={M} k={k} {dtype} eps={eps} max_iter={m}")
+
+
+@pytest.mark.parametrize("N", [1 << 16, 1 << 18, 1 << 20])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_config3_full_rows_sampled(N, dtype):
+    M, k = 256, 32
+    x = synth.make("normal", N, M, seed=0, dtype=dtype)
+    rows = _sample_rows(N, 3000)
+    for m, eps in ((-1, 0.0), (2, 0.0), (-1, 1e-2)):
+        v, i, it, st = _run(x, k, m, eps)
+        assert st == 0
+        ov, oi, oit = oracle.replay(x[rows], k, m, eps)
+        assert_same_selection(v, i, ov, oi, rows=rows, what=f"N={N} {dtype} max_iter={m} eps={eps}")
+        np.testing.assert_array_equal(it[rows], oit)
+
+
+# ---- configuration 4: long rows, adversarial values ------------------------------------
+@pytest.mark.parametrize("value_set", ["uniform", "int_ties", "all_equal", "outliers", "subnormal"])
+@pytest.mark.parametrize("M", [2048, 4096, 8192])
+def test_config4_long_rows_adversarial(M, value_set):
+    N = 65536
+    x = synth.make(value_set, N, M, seed=0)
+    rows = _sample_rows(N, 300)
+    xt = to_dev(x)
+    for k in (64, 256, 1024):
+        v, i, it, st = api.rtopk_select_stats(xt, k)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ov, oi, oit = oracle.replay(x[rows], k)
+        assert_same_selection(v, i, ov, oi, rows=rows, what=f"M={M} {value_set} k={k}")
+        np.testing.assert_array_equal(it.cpu().numpy()[rows], oit)
+        _, si = oracle.sort_topk(x[rows], k)
+        np.testing.assert_array_equal(i.cpu().numpy()[rows], si)
+    del xt
+    torch.cuda.empty_cache()
+
+
+# ---- configuration 5: fused MaxK layer, bf16 -> CBSR (int16) -> backward scatter ---------
+def test_config5_maxk_forward_backward():
+    N, M, k = 1 << 20, 256, 32
+    xb = synth.normal_bf16(N, M, seed=0)
+    xt = to_dev(xb)
+    fv, fi = api.maxk_forward(xt, k)
+    torch.cuda.synchronize()
+    assert fi.dtype == torch.int16 and fv.dtype == torch.bfloat16
+    # every row: values are the input at the kept indices, indices strictly ascending
+    fil = fi.long()
+    assert torch.equal(torch.gather(xt, 1, fil).view(torch.int16), fv.view(torch.int16))
+    assert bool((fil[:, 1:] > fil[:, :-1]).all()) and int(fil.min()) >= 0 and int(fil.max()) < M
+    rows = _sample_rows(N, 4000)
+    ov, oi, _ = oracle.replay(xb[rows], k)
+    assert_same_selection(fv, fi, ov, oi, rows=rows, what="maxk_forward")
+    # backward over all rows against the oracle scatter
+    dy = synth.normal_bf16(N, k, seed=1)
+    g = api.maxk_backward_scatter(to_dev(dy), fi, M)
+    torch.cuda.synchronize()
+    want = oracle.maxk_backward(dy, fi.cpu().numpy(), M)
+    np.testing.assert_array_equal(vals_np(g), want)
+
+
+# ---- edge cases --------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 31, 33, 100, 129, 1000, 1023, 1024, 1025, 1500,
+                               2047, 4095, 5000, 8191, 8192])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_edge_row_lengths(M, dtype):
+    N = 300
+    x = synth.make("int_ties" if M % 2 else "normal", N, M, seed=M, dtype=dtype)
+    for k in sorted({1, max(1, M // 3), M}):
+        for m in (-1, 0, 3):
+            _check_full(x, k, m, what=f"M={M} {dtype} k={k} max_iter={m}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_misaligned_input_pointer(dtype):
+    N, M, k = 257, 256, 32
+    x = synth.make("normal", N, M + 1, seed=3, dtype=dtype)
+    flat = to_dev(x).reshape(-1)
+    xt = flat[1:1 + N * M].view(N, M)  # 4- or 2-byte offset: no 16-byte loads possible
+    v, i, it, st = api.rtopk_select_stats(xt, k)
+    torch.cuda.synchronize()
+    host = x.reshape(-1)[1:1 + N * M].reshape(N, M)
+    ov, oi, oit = oracle.replay(host, k)
+    assert_same_selection(v, i, ov, oi, what="misaligned")
+    np.testing.assert_array_equal(it.cpu().numpy(), oit)
+
+
+def test_tiny_and_degenerate():
+    for N in (1, 2, 7):
+        x = synth.normal_f32(N, 256, seed=N)
+        _check_full(x, 32, what=f"N={N}")
+    x = synth.all_equal_rows_f32(100, 256, seed=1)
+    _check_full(x, 32, what="all equal")
+    x = synth.normal_f32(100, 256, seed=2)
+    _check_full(x, 32, -1, 1e30, what="eps >= range")
+    _check_full(x, 256, what="k == M")
+    # N == 0 is a no-op
+    v, i = api.rtopk_select(torch.empty((0, 256), device="cuda"), 32)
+    assert v.shape == (0, 32)
+
+
+def test_signed_zero_and_subnormal_bits():
+    x = synth.subnormals_f32(512, 256, seed=5)
+    x[:, ::7] = np.float32(-0.0)
+    x[:, 3::11] = np.float32(0.0)
+    _check_full(x, 40, what="zeros+subnormals")
+    _check_full(x, 40, 5, what="zeros+subnormals early stop")
+
+
+def test_status_word_flags_bad_rows():
+    x = synth.normal_f32(64, 256, seed=0)
+    x[3, 10] = np.nan
+    x[9, 0] = np.inf
+    x[20, 5] = np.float32(3e38)
+    v, i, it, st = _run(x, 32)
+    assert st & 0x1 and st & 0x2 and not st & 0x4
+    good = np.setdiff1d(np.arange(64), [3, 9, 20])
+    ov, oi, _ = oracle.replay(x[good], 32)
+    assert_same_selection(v, i, ov, oi, rows=good, what="good rows beside bad ones")
+
+
+def test_backward_bad_index_flag_and_edges():
+    N, M, k = 40, 100, 10
+    dy = synth.normal_bf16(N, k, seed=1)
+    idx = np.tile(np.arange(0, 3 * k, 3, dtype=np.int16), (N, 1))
+    idx[5, 2] = 100  # out of range
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = api.maxk_backward_scatter(to_dev(dy), torch.from_numpy(idx).cuda(), M, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 0x8
+    ok = np.setdiff1d(np.arange(N), [5])
+    want = oracle.maxk_backward(dy[ok], idx[ok], M)
+    np.testing.assert_array_equal(vals_np(g)[ok], want)
+    for M2 in (1, 7, 8, 8192):
+        k2 = min(4, M2)
+        dy2 = synth.normal_bf16(9, k2, seed=2)
+        idx2 = np.tile(np.arange(k2, dtype=np.int16) * (M2 // k2), (9, 1))
+        g2 = api.maxk_backward_scatter(to_dev(dy2), torch.from_numpy(idx2).cuda(), M2)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(vals_np(g2), oracle.maxk_backward(dy2, idx2, M2))
+
+
+def test_side_stream_and_determinism():
+    x = synth.normal_f32(20000, 512, seed=4)
+    xt = to_dev(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        v1, i1 = api.rtopk_select(xt, 64)
+    s.synchronize()
+    v2, i2 = api.rtopk_select(xt, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2) and torch.equal(v1.view(torch.int32), v2.view(torch.int32))
+
+
+def test_autograd_maxk_layer():
+    x = synth.normal_bf16(512, 256, seed=0)
+    xt = to_dev(x).requires_grad_(True)
+    vals, idx = api.MaxK.apply(xt, 32)
+    (vals.float() * 2).sum().backward()
+    g = xt.grad
+    ov, oi, _ = oracle.replay(x, 32)
+    two = np.full((512, 32), 0x4000, dtype=np.uint16)  # bf16 2.0
+    np.testing.assert_array_equal(vals_np(g), oracle.maxk_backward(two, oi.astype(np.int16), 256))
