@@ -384,6 +384,7 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
 
 
 def main():
+    global N_ROWS
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -394,7 +395,6 @@ def main():
     ap.add_argument("--rows", type=int, default=N_ROWS,
                     help="rows per rank (default 2^20, the metric's workload; smaller only for profiling)")
     args = ap.parse_args()
-    global N_ROWS
     N_ROWS = args.rows
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
