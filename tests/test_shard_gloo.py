@@ -60,7 +60,7 @@ def test_bench_reference_arm_two_ranks(oracle_mod):
     port = 30500 + (os.getpid() % 1000)
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
-           "--gpus", "2", "--steps", "2", "--warmup", "0"]
+           "--gpus", "2", "--steps", "2", "--warmup", "0", "--rows", "65536"]
     p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
