@@ -19,11 +19,14 @@
 //  * exact mode (max_iter < 0, eps == 0) compiles a loop with no cap or
 //    precision test beyond the safety cap (the collapse test subsumes
 //    hi - lo > 0);
-//  * the fill pass uses one prefix field per group when the search ended on
-//    c(lo) == k (everything at or above lo is kept), and the general
-//    S / borderline pair of fields otherwise;
+//  * a pass counts x >= mid from the sign bit of x - mid (one subtract on the
+//    FMA pipe and one shift-add per element);
+//  * when the search ends on c(lo) == k (the usual exact-mode ending) the
+//    fill keeps exactly {x >= lo}: one packed prefix scan of per-group counts;
+//    other endings take the general S / borderline fill, whose per-slot step
+//    is one straight-line predicated shared-memory store;
 //  * kept (value, index) pairs are staged in shared memory and written out
-//    with coalesced stores (k <= 64), else stored directly.
+//    with coalesced stores (k <= 256), else stored directly.
 // Arithmetic and branch decisions are identical to rtopk_select_kernel.
 #pragma once
 
@@ -31,7 +34,7 @@
 
 namespace rtopk {
 
-constexpr int kStageK = 64;  // per-warp shared staging of the CBSR row
+constexpr int kStageK = 256;  // per-warp shared staging of the CBSR row (k <= 256)
 
 template <typename T, int G>
 __device__ __forceinline__ void load_row_w1(const T* __restrict__ in, int64_t r, int M, int lane,
@@ -51,10 +54,51 @@ __device__ __forceinline__ unsigned warp_excl_scan(unsigned v, int lane, unsigne
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const unsigned t = __shfl_up_sync(0xffffffffu, s, d);
-    if (lane >= d) s += t;
+    s += (lane >= d) ? t : 0u;
   }
   tot = __shfl_sync(0xffffffffu, s, 31);
   return s - v;
+}
+
+// One general fill slot, straight-line: S = v >= hi is kept; B = lo <= v < hi
+// is kept while its rank among B (runB) is below `need`; position
+// runS + min(runB, need), bounded by k. Advances runS / runB.
+__device__ __forceinline__ void stage_general(float v, float lo, float hi, int need, int k, uint32_t sbase,
+                                              int& runS, int& runB, int j) {
+  asm volatile(
+      "{\n\t.reg .pred ps, pb, pn, pk;\n\t.reg .s32 m, q;\n\t.reg .u32 a;\n\t"
+      "setp.ge.f32 ps, %2, %4;\n\t"
+      "setp.ge.and.f32 pb, %2, %3, !ps;\n\t"
+      "setp.lt.and.s32 pn, %1, %5, pb;\n\t"
+      "or.pred pk, ps, pn;\n\t"
+      "min.s32 m, %1, %5;\n\t"
+      "add.s32 q, %0, m;\n\t"
+      "setp.lt.and.s32 pk, q, %6, pk;\n\t"
+      "mad.lo.u32 a, q, 8, %7;\n\t"
+      "@pk st.shared.v2.b32 [a], {%8, %9};\n\t"
+      "@ps add.s32 %0, %0, 1;\n\t"
+      "@pb add.s32 %1, %1, 1;\n\t}"
+      : "+r"(runS), "+r"(runB)
+      : "f"(v), "f"(lo), "f"(hi), "r"(need), "r"(k), "r"(sbase), "r"(__float_as_uint(v)), "r"(j)
+      : "memory");
+}
+
+// Predicated global stores (rows whose k exceeds the shared staging area).
+__device__ __forceinline__ void st_global_if(unsigned p, float* a, float v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.global.b32 [%1], %2;\n\t}"
+               ::"r"(p), "l"(a), "r"(__float_as_uint(v)) : "memory");
+}
+__device__ __forceinline__ void st_global_if(unsigned p, int32_t* a, int32_t v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.global.b32 [%1], %2;\n\t}"
+               ::"r"(p), "l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_if(unsigned p, uint16_t* a, uint16_t v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.global.b16 [%1], %2;\n\t}"
+               ::"r"(p), "l"(a), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_if(unsigned p, int16_t* a, int16_t v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.global.b16 [%1], %2;\n\t}"
+               ::"r"(p), "l"(a), "h"(v) : "memory");
 }
 
 template <typename T, int G, bool FULL, bool EXACT, typename IdxT>
@@ -90,7 +134,6 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
   if (!ok) st |= (isfinite(lo) && isfinite(hi)) ? kStatusRange : kStatusNonFinite;
 
   // ---- ties at the maximum: only possible if enough lanes hold the maximum
-  int c_lo = M;  // c(min) = every element of the row
   bool max_tie = false;
   {
     const int lanes_at_max = __popc(__ballot_sync(0xffffffffu, mx == hi));
@@ -104,13 +147,16 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
     }
   }
 
+  // ---- bisection. A pass counts x >= mid from the sign bit of x - mid
+  // (finite |x|, |mid| <= 1e38, -inf pads); a zero threshold is taken as -0
+  // so that x = -0 gives (-0) - (-0) = +0 and counts as >= (it equals +0).
   int it = 0;
+  bool eq = false;
   if (max_tie) {
     lo = hi;           // keep the k lowest-index maxima through the fill rule:
     hi = pos_inf();    // S is empty and every maximum is borderline
-    c_lo = k + 1;      // force the general fill
   } else {
-    while (true) {
+    for (;;) {
       if (EXACT) {
         if (it >= kSafetyCap) { st |= kStatusSafetyCap; break; }
       } else {
@@ -122,31 +168,37 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
       }
       const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
       if (!(lo < mid && mid < hi)) break;
-      int c = 0;
+      const float t = (mid == 0.0f) ? -0.0f : mid;
+      unsigned lt0 = 0, lt1 = 0;
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < V; ++e) c += (x[g][e] >= mid) ? 1 : 0;
-      const int cnt = int(__reduce_add_sync(0xffffffffu, unsigned(c)));
+        for (int e = 0; e < V; ++e) {
+          const unsigned sb = __float_as_uint(__fsub_rn(x[g][e], t)) >> 31;
+          if ((g * V + e) & 1) lt1 += sb; else lt0 += sb;
+        }
+      const int cnt = 32 * NE - int(__reduce_add_sync(0xffffffffu, lt0 + lt1));
       ++it;
-      if (cnt >= k) {
-        lo = mid;
-        c_lo = cnt;
-        if (cnt == k) break;
-      } else {
-        hi = mid;
-      }
+      const bool ge = cnt >= k;
+      lo = ge ? mid : lo;
+      hi = ge ? hi : mid;
+      if (cnt == k) { eq = true; break; }
     }
   }
 
-  // ---- fill pass and CBSR store
+  // ---- fill pass and CBSR store: S = {x >= hi} kept, B = {lo <= x < hi}
+  // fills the remaining k - |S| in ascending index order (branch-free: every
+  // slot issues one predicated store and advances its prefix counters)
   const int64_t obase = r * int64_t(k);
   const bool staged = (k <= kStageK);
-  if (ok && c_lo == k) {
-    // the search ended with exactly k elements at or above lo: keep them all
-    unsigned pkw[(G + FPW - 1) / FPW];
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+  const int jl = lane * V;
+  if (ok && eq && staged) {
+    // the search ended on c(lo) == k: keep exactly {x >= lo}, in index order
+    constexpr int NWF = (G + FPW - 1) / FPW;
+    unsigned pkw[NWF];
 #pragma unroll
-    for (int q = 0; q < (G + FPW - 1) / FPW; ++q) pkw[q] = 0u;
+    for (int q = 0; q < NWF; ++q) pkw[q] = 0u;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       unsigned c = 0;
@@ -156,7 +208,7 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
     }
     int base = 0;
 #pragma unroll
-    for (int q = 0; q < (G + FPW - 1) / FPW; ++q) {
+    for (int q = 0; q < NWF; ++q) {
       unsigned tot;
       const unsigned ex = warp_excl_scan(pkw[q], lane, tot);
 #pragma unroll
@@ -166,15 +218,8 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
           int pos = base + int((ex >> (FB * f)) & FMASK);
 #pragma unroll
           for (int e = 0; e < V; ++e) {
-            const float v = x[g][e];
-            if (v >= lo) {
-              const int j = g * GS + lane * V + e;
-              if (staged) {
-                stage[pos] = make_float2(v, __int_as_float(j));
-              } else {
-                vals[obase + pos] = out_value(v, vals);
-                idx[obase + pos] = IdxT(j);
-              }
+            if (x[g][e] >= lo) {
+              stage[pos] = make_float2(x[g][e], __int_as_float(g * GS + jl + e));
               ++pos;
             }
           }
@@ -182,8 +227,8 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
         }
       }
     }
-  } else {
-    // general: S = {x >= hi} kept, B = {lo <= x < hi} fills the rest by index
+  } else
+  {
     constexpr int NF = 2 * G;
     constexpr int NW = (NF + FPW - 1) / FPW;
     unsigned pkw[NW];
@@ -194,12 +239,11 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
       unsigned cs = 0, cb = 0;
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const bool s = x[g][e] >= hi;
-        cs += s ? 1u : 0u;
-        cb += (!s && x[g][e] >= lo) ? 1u : 0u;
+        cs += (x[g][e] >= hi) ? 1u : 0u;
+        cb += (x[g][e] >= lo) ? 1u : 0u;  // S and B together; B = difference
       }
       pkw[(2 * g) / FPW] += cs << (FB * ((2 * g) % FPW));
-      pkw[(2 * g + 1) / FPW] += cb << (FB * ((2 * g + 1) % FPW));
+      pkw[(2 * g + 1) / FPW] += (cb - cs) << (FB * ((2 * g + 1) % FPW));
     }
     unsigned ex[NW], tot[NW];
 #pragma unroll
@@ -217,20 +261,19 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
 #pragma unroll
       for (int e = 0; e < V; ++e) {
         const float v = x[g][e];
-        const bool s = v >= hi;
-        const bool b = !s && v >= lo;
-        const int pos = runS + min(runB, need);
-        if ((s || (b && runB < need)) && pos < k) {
-          const int j = g * GS + lane * V + e;
-          if (staged) {
-            stage[pos] = make_float2(v, __int_as_float(j));
-          } else {
-            vals[obase + pos] = out_value(v, vals);
-            idx[obase + pos] = IdxT(j);
-          }
+        const int j = g * GS + jl + e;
+        if (staged) {
+          stage_general(v, lo, hi, need, k, sbase, runS, runB, j);
+        } else {
+          const unsigned sf = (v >= hi) ? 1u : 0u;
+          const unsigned bf = (v >= lo) ? 1u - sf : 0u;
+          const int pos = runS + min(runB, need);
+          const unsigned keep = (sf | (bf & unsigned(runB < need))) & unsigned(pos < k);
+          st_global_if(keep, vals + obase + pos, out_value(v, vals));
+          st_global_if(keep, idx + obase + pos, IdxT(j));
+          runS += int(sf);
+          runB += int(bf);
         }
-        runS += s ? 1 : 0;
-        runB += b ? 1 : 0;
       }
       baseS += int((tot[fs / FPW] >> (FB * (fs % FPW))) & FMASK);
       baseB += int((tot[fb / FPW] >> (FB * (fb % FPW))) & FMASK);
