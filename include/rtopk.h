@@ -17,8 +17,11 @@
  *          "Why it works".
  *
  * Conventions shared by every entry point:
- *  - All array pointers are caller-owned DEVICE memory (e.g. torch tensors),
- *    dense and row-major: inputs have row stride M, CBSR outputs row stride k.
+ *  - All array pointers are caller-owned memory the device can address:
+ *    device memory (e.g. torch tensors), or pinned / registered host memory,
+ *    which the kernels then read and write in place over the host link
+ *    (NVLink-C2C on Grace-Blackwell) with no staging copy. Arrays are dense
+ *    and row-major: inputs have row stride M, CBSR outputs row stride k.
  *    The library allocates no memory and keeps no state between calls, except
  *    a per-device cache of the SM count and occupancy used to size grids.
  *  - Every call is asynchronous on `stream` (0 = legacy default stream).

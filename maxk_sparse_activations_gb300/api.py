@@ -3,7 +3,9 @@
 Every function here checks shapes and dtypes, allocates outputs with torch when
 the caller passes none, and calls the same-named entry point of librtopk.so on
 the current CUDA stream. All selection and scatter work runs in the library's
-CUDA kernels; nothing here computes on the host.
+CUDA kernels; nothing here computes on the host. Tensors may live in device
+memory or in pinned host memory: on a Grace-Blackwell node the kernels then
+read and write the host buffers directly over NVLink-C2C, with no staging copy.
 """
 from __future__ import annotations
 
@@ -15,15 +17,27 @@ from . import _lib
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream(device)
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if device.type != "cuda":  # pinned host tensors: the current CUDA device's stream
+        device = torch.device("cuda", torch.cuda.current_device())
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _need_cuda_2d(t: torch.Tensor, name: str) -> None:
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    """Device tensors, or pinned host tensors that the GPU reads and writes in
+    place (over NVLink-C2C / PCIe, no staging copy)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
     if t.dim() != 2 or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous 2-D tensor")
+
+
+def _empty_like_home(shape, dtype, x: torch.Tensor) -> torch.Tensor:
+    """Output in the same memory as the input: device memory, or pinned host memory."""
+    if x.is_cuda:
+        return torch.empty(shape, dtype=dtype, device=x.device)
+    return torch.empty(shape, dtype=dtype).pin_memory()
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -58,14 +72,14 @@ def rtopk_select_stats(x: torch.Tensor, k: int, max_iter: int = -1, eps: float =
         raise ValueError("x must be float32 or bfloat16")
     N, M = x.shape
     if vals is None:
-        vals = torch.empty((N, k), dtype=x.dtype, device=x.device)
+        vals = _empty_like_home((N, k), x.dtype, x)
     if idx is None:
-        idx = torch.empty((N, k), dtype=torch.int32, device=x.device)
+        idx = _empty_like_home((N, k), torch.int32, x)
     if stats:
         if iters is None:
-            iters = torch.empty((N,), dtype=torch.int32, device=x.device)
+            iters = _empty_like_home((N,), torch.int32, x)
         if status is None:
-            status = torch.zeros((1,), dtype=torch.int32, device=x.device)
+            status = _empty_like_home((1,), torch.int32, x).zero_()
     lib = _lib.load()
     if stats:
         rc = lib.rtopk_select_stats(x.data_ptr(), N, M, int(k), int(max_iter), float(eps), dtype,
@@ -87,9 +101,9 @@ def maxk_forward(x: torch.Tensor, k: int, max_iter: int = -1, eps: float = 0.0, 
         raise ValueError("maxk_forward takes bfloat16 input")
     N, M = x.shape
     if vals is None:
-        vals = torch.empty((N, k), dtype=torch.bfloat16, device=x.device)
+        vals = _empty_like_home((N, k), torch.bfloat16, x)
     if idx is None:
-        idx = torch.empty((N, k), dtype=torch.int16, device=x.device)
+        idx = _empty_like_home((N, k), torch.int16, x)
     rc = _lib.load().maxk_forward(x.data_ptr(), N, M, int(k), int(max_iter), float(eps),
                                   vals.data_ptr(), idx.data_ptr(), _stream_ptr(stream, x.device))
     _lib.check(rc, "maxk_forward")
@@ -108,7 +122,7 @@ def maxk_backward_scatter(dy: torch.Tensor, idx: torch.Tensor, M: int, *,
         raise ValueError("dy and idx must have the same N x k shape")
     N, k = dy.shape
     if grad is None:
-        grad = torch.empty((N, M), dtype=torch.bfloat16, device=dy.device)
+        grad = _empty_like_home((N, M), torch.bfloat16, dy)
     rc = _lib.load().maxk_backward_scatter(dy.data_ptr(), idx.data_ptr(), N, int(M), int(k),
                                            grad.data_ptr(), _ptr(status), _stream_ptr(stream, dy.device))
     _lib.check(rc, "maxk_backward_scatter")

@@ -240,3 +240,20 @@ def test_autograd_maxk_layer():
     ov, oi, _ = oracle.replay(x, 32)
     two = np.full((512, 32), 0x4000, dtype=np.uint16)  # bf16 2.0
     np.testing.assert_array_equal(vals_np(g), oracle.maxk_backward(two, oi.astype(np.int16), 256))
+
+
+def test_pinned_host_buffers_zero_copy():
+    """The kernels read and write pinned host memory in place (no staging copy)."""
+    x = synth.normal_f32(5000, 256, seed=12)
+    xh = torch.from_numpy(x).pin_memory()
+    v, i = api.rtopk_select(xh, 32)
+    torch.cuda.synchronize()
+    assert not v.is_cuda and v.is_pinned() and i.is_pinned()
+    ov, oi, _ = oracle.replay(x, 32)
+    assert_same_selection(v.numpy().view(np.uint32), i.numpy(), ov, oi, what="pinned host")
+    xb = synth.normal_bf16(3000, 256, seed=13)
+    xbh = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory()
+    fv, fi = api.maxk_forward(xbh, 32)
+    torch.cuda.synchronize()
+    bv, bi, _ = oracle.replay(xb, 32)
+    assert_same_selection(fv.view(torch.int16).numpy().view(np.uint16), fi.numpy(), bv, bi, what="pinned bf16")
