@@ -3,39 +3,63 @@
 
 #include "launch.h"
 #include "rtopk_select.cuh"
-#include "rtopk_warp.cuh"
+#include "rtopk_block.cuh"
 
 namespace rtopk {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// One warp per row (W = 1): exact-mode and general loops, full and padded rows.
+// One warp per row (W = 1). L = compaction list entries per lane (0 = off).
+// Measured on GB300 (2^18 N(0,1) rows): compaction costs more than it saves
+// while a lane holds few elements (M = 256: 187 vs 160 us), and pays from 32
+// elements per lane (M = 1024, k = 32: 358 vs 392 us with L = 4; M = 2048,
+// k = 64: 849 vs 917 us with L = 8).
 template <typename T, int G, typename IdxT>
 cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s) {
   constexpr int kThreads = 256;
+  constexpr int NE = G * ElemTraits<T>::V;
   const bool exact = a.max_iter < 0 && a.eps == 0.0f;
-  auto kern = full ? (exact ? rtopk_warp_kernel<T, G, true, true, IdxT> : rtopk_warp_kernel<T, G, true, false, IdxT>)
-                   : (exact ? rtopk_warp_kernel<T, G, false, true, IdxT> : rtopk_warp_kernel<T, G, false, false, IdxT>);
+  const int L = (NE >= 64 && a.k <= 128) ? 8 : ((NE >= 32 && a.k <= 64) ? 4 : 0);
+  using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);
+  K kern;
+  if (L == 4) {
+    kern = exact ? rtopk_warp_kernel<T, G, true, (NE >= 32 ? 4 : 0), IdxT>
+                 : rtopk_warp_kernel<T, G, false, (NE >= 32 ? 4 : 0), IdxT>;
+  } else if (L == 8) {
+    kern = exact ? rtopk_warp_kernel<T, G, true, (NE >= 64 ? 8 : 0), IdxT>
+                 : rtopk_warp_kernel<T, G, false, (NE >= 64 ? 8 : 0), IdxT>;
+  } else {
+    kern = exact ? rtopk_warp_kernel<T, G, true, 0, IdxT> : rtopk_warp_kernel<T, G, false, 0, IdxT>;
+  }
   const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), kThreads, 0, (a.N + 7) / 8);
   if (blocks <= 0) return cudaErrorInvalidConfiguration;
-  kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, a.max_iter, a.eps, vec,
+  kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, a.max_iter, a.eps, full, vec,
                                    static_cast<T*>(a.vals), static_cast<IdxT*>(a.idx), a.iters, a.status);
   return cudaGetLastError();
 }
 
-// One 256-thread block per row (W = 8) for rows longer than 1024 elements.
+// One 256-thread block per row for rows longer than kWarpMaxM elements;
+// LB = 8 hands the tail of the search to warp 0 once c(lo) <= 256.
 template <typename T, int G, typename IdxT>
 cudaError_t launch_block(const SelectArgs& a, bool full, bool vec, cudaStream_t s) {
   constexpr int kThreads = 256;
-  auto kern = full ? rtopk_select_kernel<T, G, 8, true, IdxT> : rtopk_select_kernel<T, G, 8, false, IdxT>;
+  const bool exact = a.max_iter < 0 && a.eps == 0.0f;
+  const bool list = 2 * a.k <= kBlockList;
+  using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);
+  K kern = list ? (exact ? rtopk_block_kernel<T, G, true, 8, IdxT> : rtopk_block_kernel<T, G, false, 8, IdxT>)
+                : (exact ? rtopk_block_kernel<T, G, true, 0, IdxT> : rtopk_block_kernel<T, G, false, 0, IdxT>);
   const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), kThreads, 0, a.N);
   if (blocks <= 0) return cudaErrorInvalidConfiguration;
-  kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, a.max_iter, a.eps, vec,
+  kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, a.max_iter, a.eps, full, vec,
                                    static_cast<T*>(a.vals), static_cast<IdxT*>(a.idx), a.iters, a.status);
   return cudaGetLastError();
 }
 
-// Row-length dispatch for rows <= 1024 elements (one warp per row).
+// Row-length dispatch for rows <= kWarpMaxM elements (one warp per row).
+#ifndef RTOPK_WARP_MAX_M
+#define RTOPK_WARP_MAX_M 2048
+#endif
+constexpr int kWarpMaxM = RTOPK_WARP_MAX_M;
 template <typename T, typename IdxT>
 cudaError_t launch_short_rows(const SelectArgs& a, cudaStream_t s) {
   constexpr int V = ElemTraits<T>::V;
@@ -43,34 +67,36 @@ cudaError_t launch_short_rows(const SelectArgs& a, cudaStream_t s) {
   const int M = a.M;
   const bool vec = (M % V == 0) && aligned16(a.in);
   const int need = (M + GS - 1) / GS;
-  const int G = need <= 4 ? need : (need <= 6 ? 6 : 8);
+  const int G = need <= 4 ? need : (need <= 6 ? 6 : (need <= 8 ? 8 : (need <= 12 ? 12 : 16)));
   const bool full = vec && M == G * GS;
   switch (G) {
     case 1: return launch_warp<T, 1, IdxT>(a, full, vec, s);
     case 2: return launch_warp<T, 2, IdxT>(a, full, vec, s);
     case 3: return launch_warp<T, 3, IdxT>(a, full, vec, s);
     case 4: return launch_warp<T, 4, IdxT>(a, full, vec, s);
-    case 6:
-      if constexpr (GS * 6 <= 1024 + GS) return launch_warp<T, 6, IdxT>(a, full, vec, s);
+    case 6: return launch_warp<T, 6, IdxT>(a, full, vec, s);
+    case 8: return launch_warp<T, 8, IdxT>(a, full, vec, s);
+    case 12:
+      if constexpr (GS * 12 <= kWarpMaxM) return launch_warp<T, 12, IdxT>(a, full, vec, s);
       return cudaErrorInvalidValue;
     default:
-      if constexpr (GS * 8 <= 1024) return launch_warp<T, 8, IdxT>(a, full, vec, s);
+      if constexpr (GS * 16 <= kWarpMaxM) return launch_warp<T, 16, IdxT>(a, full, vec, s);
       return cudaErrorInvalidValue;
   }
 }
 
-// Row-length dispatch for 1024 < M <= 8192 (one block per row).
+// Row-length dispatch for kWarpMaxM < M <= 8192 (one block per row).
 template <typename T, typename IdxT>
 cudaError_t launch_long_rows(const SelectArgs& a, cudaStream_t s) {
   constexpr int V = ElemTraits<T>::V;
-  constexpr int GS = 32 * V * 8;  // elements per group across the block
+  constexpr int GS = 32 * V * kBlockWarps;  // elements per group across the block
   const int M = a.M;
   const bool vec = (M % V == 0) && aligned16(a.in);
   const int need = (M + GS - 1) / GS;
   const int G = need <= 4 ? need : (need <= 6 ? 6 : 8);
   const bool full = vec && M == G * GS;
   switch (G) {
-    case 1: return launch_block<T, 1, IdxT>(a, full, vec, s);
+    case 1:
     case 2: return launch_block<T, 2, IdxT>(a, full, vec, s);
     case 3: return launch_block<T, 3, IdxT>(a, full, vec, s);
     case 4: return launch_block<T, 4, IdxT>(a, full, vec, s);

@@ -1,4 +1,4 @@
-// Row-wise top-k, one warp per row (rows up to 1024 elements), sm_103a.
+// Row-wise top-k, one warp per row (rows up to 2048 elements), sm_103a.
 //
 // Source: "RTop-K: Ultra-Fast Row-Wise Top-K Selection for Neural Network
 // Acceleration on GPUs" (summary page), "Approach" (binary search over each
@@ -8,26 +8,30 @@
 // Accelerating Graph Neural Networks Training", "The idea" (CBSR: dense N x k
 // values and indices).
 //
-// This is the instruction-lean variant of rtopk_select_kernel for W = 1. The
-// search is issue-bound (about 8 passes over the row per N(0,1) row at
-// M = 256), so everything around the passes is trimmed:
-//  * the next row is loaded into a second register set while the current row
-//    is searched (one row of HBM traffic always in flight per warp);
-//  * the maximum-tie pass runs only when enough lanes hold the maximum for
-//    c(max) >= k to be possible (a ballot bounds it), which for continuous
-//    data is almost never;
-//  * exact mode (max_iter < 0, eps == 0) compiles a loop with no cap or
-//    precision test beyond the safety cap (the collapse test subsumes
-//    hi - lo > 0);
+// The search is issue-bound (about 8 passes over the row per N(0,1) row at
+// M = 256), so the kernel is built around instruction count:
+//  * the row lives in registers (lane l holds 16 bytes of each 32*V-element
+//    group), one row per warp, no second register set: occupancy hides the
+//    load latency better than a register prefetch;
 //  * a pass counts x >= mid from the sign bit of x - mid (one subtract on the
 //    FMA pipe and one shift-add per element);
-//  * when the search ends on c(lo) == k (the usual exact-mode ending) the
-//    fill keeps exactly {x >= lo}: one packed prefix scan of per-group counts;
-//    other endings take the general S / borderline fill, whose per-slot step
-//    is one straight-line predicated shared-memory store;
+//  * the maximum-tie pass runs only when enough lanes hold the maximum for
+//    c(max) >= k to be possible (a ballot bounds it);
+//  * exact mode (max_iter < 0, eps == 0) compiles a loop without the cap and
+//    precision tests (the collapse test subsumes hi - lo > 0);
+//  * compaction (L > 0): once c(lo) <= 32 L, the elements >= lo -- a superset
+//    of every later candidate -- are written in index order to a per-warp
+//    list, and the remaining passes count L list entries per lane instead of
+//    the whole row; the CBSR row then comes straight from the list through
+//    warp ballots. Counts, passes and results are unchanged: c(mid) over the
+//    list equals c(mid) over the row for every mid > lo;
+//  * when the search ends on c(lo) == k the kept set is exactly {x >= lo}: one
+//    packed prefix scan of per-group counts places it; other endings take the
+//    general S / borderline fill;
 //  * kept (value, index) pairs are staged in shared memory and written out
 //    with coalesced stores (k <= 256), else stored directly.
-// Arithmetic and branch decisions are identical to rtopk_select_kernel.
+// Arithmetic and branch decisions are identical to the scalar definition of
+// the method (and to rtopk_select_kernel).
 #pragma once
 
 #include "rtopk_select.cuh"
@@ -101,12 +105,154 @@ __device__ __forceinline__ void st_global_if(unsigned p, int16_t* a, int16_t v) 
                ::"r"(p), "l"(a), "h"(v) : "memory");
 }
 
-template <typename T, int G, bool FULL, bool EXACT, typename IdxT>
-__device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>::V], int64_t r, int M,
-                                               int k, int limit, bool cap_is_safety, float eps, int lane,
+// Count of this lane's x < t over the registers, t = mid with +0 taken as -0.
+template <int G, int V>
+__device__ __forceinline__ unsigned lane_count_lt(const float (&x)[G][V], float mid) {
+  const float t = (mid == 0.0f) ? -0.0f : mid;
+  unsigned lt0 = 0, lt1 = 0;
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      const unsigned sb = __float_as_uint(__fsub_rn(x[g][e], t)) >> 31;
+      if ((g * V + e) & 1) lt1 += sb; else lt0 += sb;
+    }
+  return lt0 + lt1;
+}
+
+// Bisection passes from the current (lo, hi); `count_lt_team(mid)` returns the
+// number of the team's elements below mid (identical in every thread), so a
+// pass count is total - count_lt_team(mid). Returns true when a pass found
+// c(mid) == k. With L > 0 it also stops (returning false, comp = true) right
+// after a pass that moved lo to a value with k < c(lo) <= 32 L.
+template <bool EXACT, int L, typename CountLtTeam>
+__device__ __forceinline__ bool search_passes(CountLtTeam count_lt_team, int total, int k, int limit,
+                                              bool cap_is_safety,
+                                              float eps, float& lo, float& hi, int& it, int& c_lo, bool& comp,
+                                              uint32_t& st) {
+  for (;;) {
+    if (EXACT) {
+      if (it >= kSafetyCap) { st |= kStatusSafetyCap; return false; }
+    } else {
+      if (it >= limit) {
+        if (cap_is_safety) st |= kStatusSafetyCap;
+        return false;
+      }
+      if (!(__fsub_rn(hi, lo) > eps)) return false;
+    }
+    const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
+    if (!(lo < mid && mid < hi)) return false;
+    const int cnt = total - int(count_lt_team(mid));
+    ++it;
+    const bool ge = cnt >= k;
+    lo = ge ? mid : lo;
+    hi = ge ? hi : mid;
+    c_lo = ge ? cnt : c_lo;
+    if (cnt == k) return true;
+    if (L > 0 && ge && cnt <= 32 * L) { comp = true; return false; }
+  }
+}
+
+// Writes the elements x >= lo of the row, in ascending index order, as
+// (value, index) pairs to stage[0 .. c(lo)).
+template <int G, int V>
+__device__ __forceinline__ void compact_ge(const float (&x)[G][V], float lo, int lane, float2* __restrict__ stage) {
+  constexpr int GS = 32 * V;
+  constexpr int FB = (GS <= 255) ? 8 : 16;
+  constexpr int FPW = 32 / FB;
+  constexpr unsigned FMASK = (1u << FB) - 1u;
+  constexpr int NWF = (G + FPW - 1) / FPW;
+  unsigned pkw[NWF];
+#pragma unroll
+  for (int q = 0; q < NWF; ++q) pkw[q] = 0u;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    unsigned c = 0;
+#pragma unroll
+    for (int e = 0; e < V; ++e) c += (x[g][e] >= lo) ? 1u : 0u;
+    pkw[g / FPW] += c << (FB * (g % FPW));
+  }
+  const int jl = lane * V;
+  int base = 0;
+#pragma unroll
+  for (int q = 0; q < NWF; ++q) {
+    unsigned tot;
+    const unsigned ex = warp_excl_scan(pkw[q], lane, tot);
+#pragma unroll
+    for (int f = 0; f < FPW; ++f) {
+      const int g = q * FPW + f;
+      if (g < G) {
+        int pos = base + int((ex >> (FB * f)) & FMASK);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          if (x[g][e] >= lo) {
+            stage[pos] = make_float2(x[g][e], __int_as_float(g * GS + jl + e));
+            ++pos;
+          }
+        }
+        base += int((tot >> (FB * f)) & FMASK);
+      }
+    }
+  }
+}
+
+// Finishes a row from its compacted list: the n (<= 32 L) elements >= lo in
+// ascending index order, as (value, index) pairs in shared memory. Runs the
+// remaining passes over the list (each lane holds entries lane + 32 s) and
+// writes the CBSR row: S = {v >= hi} kept, B = {lo <= v < hi} fills the rest
+// by index -- entry order is index order, so warp ballots give the ranks.
+template <bool EXACT, int L, typename T, typename IdxT>
+__device__ __forceinline__ void finish_from_list(const float2* __restrict__ list, int n, float lo, float hi,
+                                                 int& it, int k, int limit, bool cap_is_safety, float eps,
+                                                 int lane, T* __restrict__ vals, IdxT* __restrict__ idx,
+                                                 int64_t obase, uint32_t& st) {
+  float lv[L][1];
+  int lj[L];
+#pragma unroll
+  for (int s = 0; s < L; ++s) {
+    const int e = s * 32 + lane;
+    const float2 p = (e < n) ? list[e] : make_float2(neg_inf(), 0.0f);
+    lv[s][0] = p.x;
+    lj[s] = __float_as_int(p.y);
+  }
+  int c_lo = n;
+  bool dummy = false;
+  search_passes<EXACT, 0>([&](float mid) { return __reduce_add_sync(0xffffffffu, lane_count_lt<L, 1>(lv, mid)); }, 32 * L, k, limit,
+                          cap_is_safety, eps, lo, hi, it, c_lo, dummy, st);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  unsigned bS[L], bB[L];
+  int sizeS = 0;
+#pragma unroll
+  for (int s = 0; s < L; ++s) {
+    const bool sf = lv[s][0] >= hi;
+    const bool af = lv[s][0] >= lo;
+    bS[s] = __ballot_sync(0xffffffffu, sf);
+    bB[s] = __ballot_sync(0xffffffffu, af && !sf);
+    sizeS += __popc(bS[s]);
+  }
+  const int need = max(k - sizeS, 0);
+  int runS = 0, runB = 0;
+#pragma unroll
+  for (int s = 0; s < L; ++s) {
+    const int rS = runS + __popc(bS[s] & lt_mask);
+    const int rB = runB + __popc(bB[s] & lt_mask);
+    const bool sf = (bS[s] >> lane) & 1u;
+    const bool bf = (bB[s] >> lane) & 1u;
+    const int pos = rS + min(rB, need);
+    if ((sf || (bf && rB < need)) && pos < k) {
+      vals[obase + pos] = out_value(lv[s][0], vals);
+      idx[obase + pos] = IdxT(lj[s]);
+    }
+    runS += __popc(bS[s]);
+    runB += __popc(bB[s]);
+  }
+}
+
+template <typename T, int G, bool EXACT, int L, typename IdxT>
+__device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>::V], bool full, int64_t r,
+                                               int M, int k, int limit, bool cap_is_safety, float eps, int lane,
                                                float2* __restrict__ stage, T* __restrict__ vals,
-                                               IdxT* __restrict__ idx, int* __restrict__ iters,
-                                               uint32_t& st) {
+                                               IdxT* __restrict__ idx, int* __restrict__ iters, uint32_t& st) {
   constexpr int V = ElemTraits<T>::V;
   constexpr int GS = 32 * V;
   constexpr int NE = G * V;
@@ -121,114 +267,58 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
 #pragma unroll
     for (int e = 0; e < V; ++e) {
       mx = max_nan(mx, x[g][e]);
-      if (FULL) {
-        mn = min_nan(mn, x[g][e]);
-      } else {
-        mn = min_nan(mn, (g * GS + lane * V + e < M) ? x[g][e] : pos_inf());
-      }
+      mn = min_nan(mn, (full || g * GS + lane * V + e < M) ? x[g][e] : pos_inf());
     }
-  const float hi0 = o2f(__reduce_max_sync(0xffffffffu, f2o(mx)));
-  const float lo0 = o2f(__reduce_min_sync(0xffffffffu, f2o(mn)));
-  float lo = lo0, hi = hi0;
+  float hi = o2f(__reduce_max_sync(0xffffffffu, f2o(mx)));
+  float lo = o2f(__reduce_min_sync(0xffffffffu, f2o(mn)));
   const bool ok = (lo >= -1e38f && hi <= 1e38f);
   if (!ok) st |= (isfinite(lo) && isfinite(hi)) ? kStatusRange : kStatusNonFinite;
 
   // ---- ties at the maximum: only possible if enough lanes hold the maximum
   bool max_tie = false;
-  {
-    const int lanes_at_max = __popc(__ballot_sync(0xffffffffu, mx == hi));
-    if (lanes_at_max * NE >= k) {
-      int c = 0;
+  if (__popc(__ballot_sync(0xffffffffu, mx == hi)) * NE >= k) {
+    int c = 0;
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < V; ++e) c += (x[g][e] >= hi) ? 1 : 0;
-      max_tie = int(__reduce_add_sync(0xffffffffu, unsigned(c))) >= k;
-    }
+      for (int e = 0; e < V; ++e) c += (x[g][e] >= hi) ? 1 : 0;
+    max_tie = int(__reduce_add_sync(0xffffffffu, unsigned(c))) >= k;
   }
 
-  // ---- bisection. A pass counts x >= mid from the sign bit of x - mid
-  // (finite |x|, |mid| <= 1e38, -inf pads); a zero threshold is taken as -0
-  // so that x = -0 gives (-0) - (-0) = +0 and counts as >= (it equals +0).
   int it = 0;
-  bool eq = false;
+  bool eq = false, comp = false;
+  int c_lo = M;
   if (max_tie) {
     lo = hi;           // keep the k lowest-index maxima through the fill rule:
     hi = pos_inf();    // S is empty and every maximum is borderline
   } else {
-    for (;;) {
-      if (EXACT) {
-        if (it >= kSafetyCap) { st |= kStatusSafetyCap; break; }
-      } else {
-        if (it >= limit) {
-          if (cap_is_safety) st |= kStatusSafetyCap;
-          break;
-        }
-        if (!(__fsub_rn(hi, lo) > eps)) break;
-      }
-      const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
-      if (!(lo < mid && mid < hi)) break;
-      const float t = (mid == 0.0f) ? -0.0f : mid;
-      unsigned lt0 = 0, lt1 = 0;
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const unsigned sb = __float_as_uint(__fsub_rn(x[g][e], t)) >> 31;
-          if ((g * V + e) & 1) lt1 += sb; else lt0 += sb;
-        }
-      const int cnt = 32 * NE - int(__reduce_add_sync(0xffffffffu, lt0 + lt1));
-      ++it;
-      const bool ge = cnt >= k;
-      lo = ge ? mid : lo;
-      hi = ge ? hi : mid;
-      if (cnt == k) { eq = true; break; }
-    }
+    eq = search_passes<EXACT, L>([&](float mid) { return __reduce_add_sync(0xffffffffu, lane_count_lt<G, V>(x, mid)); }, 32 * NE, k, limit,
+                                 cap_is_safety, eps, lo, hi, it, c_lo, comp, st);
   }
+  comp = comp && ok;
 
-  // ---- fill pass and CBSR store: S = {x >= hi} kept, B = {lo <= x < hi}
-  // fills the remaining k - |S| in ascending index order (branch-free: every
-  // slot issues one predicated store and advances its prefix counters)
   const int64_t obase = r * int64_t(k);
   const bool staged = (k <= kStageK);
-  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
-  const int jl = lane * V;
+  if (L > 0 && comp) {
+    // ---- compacted phase: list of the c(lo) <= 32 L elements >= lo
+    compact_ge<G, V>(x, lo, lane, stage);
+    __syncwarp();
+    finish_from_list<EXACT, (L > 0 ? L : 1), T, IdxT>(stage, c_lo, lo, hi, it, k, limit, cap_is_safety, eps,
+                                                     lane, vals, idx, obase, st);
+    __syncwarp();
+    if (iters != nullptr && lane == 0) iters[r] = it;
+    return;
+  }
+
+  // ---- fill pass and CBSR store
   if (ok && eq && staged) {
     // the search ended on c(lo) == k: keep exactly {x >= lo}, in index order
-    constexpr int NWF = (G + FPW - 1) / FPW;
-    unsigned pkw[NWF];
-#pragma unroll
-    for (int q = 0; q < NWF; ++q) pkw[q] = 0u;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      unsigned c = 0;
-#pragma unroll
-      for (int e = 0; e < V; ++e) c += (x[g][e] >= lo) ? 1u : 0u;
-      pkw[g / FPW] += c << (FB * (g % FPW));
-    }
-    int base = 0;
-#pragma unroll
-    for (int q = 0; q < NWF; ++q) {
-      unsigned tot;
-      const unsigned ex = warp_excl_scan(pkw[q], lane, tot);
-#pragma unroll
-      for (int f = 0; f < FPW; ++f) {
-        const int g = q * FPW + f;
-        if (g < G) {
-          int pos = base + int((ex >> (FB * f)) & FMASK);
-#pragma unroll
-          for (int e = 0; e < V; ++e) {
-            if (x[g][e] >= lo) {
-              stage[pos] = make_float2(x[g][e], __int_as_float(g * GS + jl + e));
-              ++pos;
-            }
-          }
-          base += int((tot >> (FB * f)) & FMASK);
-        }
-      }
-    }
-  } else
-  {
+    compact_ge<G, V>(x, lo, lane, stage);
+  } else {
+    // general: S = {x >= hi} kept, B = {lo <= x < hi} fills the remaining
+    // k - |S| in ascending index order
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+    const int jl = lane * V;
     constexpr int NF = 2 * G;
     constexpr int NW = (NF + FPW - 1) / FPW;
     unsigned pkw[NW];
@@ -291,10 +381,16 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
   if (iters != nullptr && lane == 0) iters[r] = it;
 }
 
-template <typename T, int G, bool FULL, bool EXACT, typename IdxT>
-__global__ void __launch_bounds__(256)
-rtopk_warp_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_iter, float eps, bool vec,
-                  T* __restrict__ vals, IdxT* __restrict__ idx, int* __restrict__ iters,
+// Minimum resident blocks per SM for a row of NE elements per lane.
+template <int NE>
+struct WarpOcc {
+  static constexpr int value = NE <= 8 ? 5 : (NE <= 16 ? 3 : (NE <= 32 ? 2 : 1));
+};
+
+template <typename T, int G, bool EXACT, int L, typename IdxT>
+__global__ void __launch_bounds__(256, WarpOcc<G * ElemTraits<T>::V>::value)
+rtopk_warp_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_iter, float eps, bool full,
+                  bool vec, T* __restrict__ vals, IdxT* __restrict__ idx, int* __restrict__ iters,
                   uint32_t* __restrict__ status) {
   constexpr int V = ElemTraits<T>::V;
   __shared__ float2 stage_all[8][kStageK];
@@ -302,23 +398,14 @@ rtopk_warp_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_ite
   const int wib = threadIdx.x >> 5;
   float2* stage = stage_all[wib];
   const int64_t nwarps = int64_t(gridDim.x) * 8;
-  int64_t r = int64_t(blockIdx.x) * 8 + wib;
   const bool cap_is_safety = (max_iter < 0 || max_iter > kSafetyCap);
   const int limit = cap_is_safety ? kSafetyCap : max_iter;
   uint32_t st = 0;
-
-  float xa[G][V], xb[G][V];
-  if (r < N) load_row_w1<T, G>(in, r, M, lane, FULL, vec, xa);
-  while (r < N) {
-    int64_t rn = r + nwarps;
-    if (rn < N) load_row_w1<T, G>(in, rn, M, lane, FULL, vec, xb);
-    process_row_w1<T, G, FULL, EXACT, IdxT>(xa, r, M, k, limit, cap_is_safety, eps, lane, stage, vals, idx, iters, st);
-    r = rn;
-    if (r >= N) break;
-    rn = r + nwarps;
-    if (rn < N) load_row_w1<T, G>(in, rn, M, lane, FULL, vec, xa);
-    process_row_w1<T, G, FULL, EXACT, IdxT>(xb, r, M, k, limit, cap_is_safety, eps, lane, stage, vals, idx, iters, st);
-    r = rn;
+  for (int64_t r = int64_t(blockIdx.x) * 8 + wib; r < N; r += nwarps) {
+    float x[G][V];
+    load_row_w1<T, G>(in, r, M, lane, full, vec, x);
+    process_row_w1<T, G, EXACT, L, IdxT>(x, full, r, M, k, limit, cap_is_safety, eps, lane, stage, vals, idx,
+                                         iters, st);
   }
   if (status != nullptr && st != 0u && lane == 0) atomicOr(status, st);
 }
