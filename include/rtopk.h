@@ -65,9 +65,11 @@ extern "C" {
 #define RTOPK_STATUS_NONFINITE  0x1u /* a row holds NaN or +-Inf */
 #define RTOPK_STATUS_RANGE      0x2u /* a row holds a finite value with |x| > 1e38 */
 #define RTOPK_STATUS_SAFETY_CAP 0x4u /* a search reached 512 passes (cannot happen for valid rows) */
-#define RTOPK_STATUS_BAD_INDEX  0x8u /* backward: an index outside [0, M) was skipped */
+#define RTOPK_STATUS_BAD_INDEX  0x8u /* an sp_index entry outside [0, M) was skipped */
+#define RTOPK_STATUS_BAD_EDGE   0x10u /* aggregation: an edge endpoint outside its row range was skipped */
 
 #define RTOPK_MAX_M 8192 /* [RTopK] "Limitations": rows longer than 8192 are unsupported */
+#define RTOPK_GNN_MAX_K 256 /* largest k of the aggregation entry points */
 
 typedef enum {
   RTOPK_F32 = 0,  /* IEEE binary32 */
@@ -142,6 +144,53 @@ int maxk_forward(const void* in_bf16, int64_t N, int32_t M, int32_t k, int32_t m
  */
 int maxk_backward_scatter(const void* dy_bf16, const int16_t* idx, int64_t N, int32_t M,
                           int32_t k, void* grad_bf16, uint32_t* status, cudaStream_t stream);
+
+/*
+ * maxk_spgemm_forward -- MaxK-GNN forward feature aggregation over CBSR: a
+ * row-wise-product SpGEMM of the graph with the compressed feature rows.
+ * [MaxK] "How MaxK-GNN works" (row-wise product with shared-memory
+ * scatter-accumulation, one global write per row), "Why it works".
+ *
+ *  out[i, m] = sum over the edges e of destination row i, in edge order, of
+ *              edge_w[e] * v for every CBSR entry (v, m) of source row
+ *              col_idx[e]; binary32 products and sums, one rounding each, no
+ *              FMA -- results are deterministic and order-exact.
+ *
+ *  row_ptr      device, n_dst + 1 int64: CSR offsets over destination rows
+ *  col_idx      device, E int32: source row of each edge (0 <= j < n_src)
+ *  edge_w       device, E fp32, or NULL for weight 1
+ *  sp_data_bf16 device, n_src x k bf16: CBSR values (e.g. from maxk_forward)
+ *  sp_index     device, n_src x k int16: CBSR columns, distinct within a row
+ *  M, k         feature width (1..8192) and kept per row (1..min(M, 256))
+ *  out          device, n_dst x M fp32, written in full
+ *  status       device uint32 or NULL: RTOPK_STATUS_BAD_EDGE / _BAD_INDEX
+ */
+int maxk_spgemm_forward(const int64_t* row_ptr, const int32_t* col_idx, const float* edge_w, int64_t n_dst,
+                        int64_t n_src, const void* sp_data_bf16, const int16_t* sp_index, int32_t M, int32_t k,
+                        float* out, uint32_t* status, cudaStream_t stream);
+
+/*
+ * maxk_sspmm_backward -- MaxK-GNN backward of the aggregation: the gradient of
+ * each CBSR value, a product sampled only at the forward sp_index.
+ * [MaxK] "Asymmetric passes, one mask" (the sp_index computed forward is
+ * reused backward; output positions are known before the kernel starts).
+ *
+ *  d_sp_data[j, t] = sum over the edges e of source row j in the transposed
+ *              graph (t_row_ptr / t_dst / t_edge_w, edges in the order given),
+ *              of t_edge_w[e] * dout[t_dst[e], sp_index[j, t]]; binary32, one
+ *              rounding per product and sum, no FMA.
+ *
+ *  t_row_ptr   device, n_src + 1 int64: CSR offsets of the transposed graph
+ *  t_dst       device, E int32: destination row of each edge (0 <= i < n_dst)
+ *  t_edge_w    device, E fp32, or NULL for weight 1
+ *  dout        device, n_dst x M fp32: gradient of the aggregation output
+ *  sp_index    device, n_src x k int16: the forward CBSR columns
+ *  d_sp_data   device, n_src x k fp32, written in full
+ *  status      device uint32 or NULL: RTOPK_STATUS_BAD_EDGE / _BAD_INDEX
+ */
+int maxk_sspmm_backward(const int64_t* t_row_ptr, const int32_t* t_dst, const float* t_edge_w, int64_t n_src,
+                        int64_t n_dst, const float* dout, const int16_t* sp_index, int32_t M, int32_t k,
+                        float* d_sp_data, uint32_t* status, cudaStream_t stream);
 
 /* Human-readable text for an rtopk_status code (static storage, never NULL). */
 const char* rtopk_strerror(int code);

@@ -20,10 +20,11 @@ STATUS_NONFINITE = 0x1
 STATUS_RANGE = 0x2
 STATUS_SAFETY_CAP = 0x4
 STATUS_BAD_INDEX = 0x8
+STATUS_BAD_EDGE = 0x10
 
 #: every symbol include/rtopk.h declares
 EXPORTED = ("rtopk_select", "rtopk_select_stats", "maxk_forward", "maxk_backward_scatter",
-            "rtopk_strerror", "rtopk_version")
+            "maxk_spgemm_forward", "maxk_sspmm_backward", "rtopk_strerror", "rtopk_version")
 
 
 def load(build_if_stale: bool = True) -> ctypes.CDLL:
@@ -46,11 +47,13 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         lib.rtopk_select_stats.argtypes = [p, i64, i32, i32, i32, f32, i32, p, p, p, p, p]
         lib.maxk_forward.argtypes = [p, i64, i32, i32, i32, f32, p, p, p]
         lib.maxk_backward_scatter.argtypes = [p, p, i64, i32, i32, p, p, p]
+        lib.maxk_spgemm_forward.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p, p, p]
+        lib.maxk_sspmm_backward.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p, p, p]
         lib.rtopk_strerror.argtypes = [ctypes.c_int]
         lib.rtopk_strerror.restype = ctypes.c_char_p
         lib.rtopk_version.argtypes = []
         for name in ("rtopk_select", "rtopk_select_stats", "maxk_forward", "maxk_backward_scatter",
-                     "rtopk_version"):
+                     "maxk_spgemm_forward", "maxk_sspmm_backward", "rtopk_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

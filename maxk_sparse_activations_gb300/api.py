@@ -145,3 +145,61 @@ class MaxK(torch.autograd.Function):
     def backward(ctx, dvals: torch.Tensor, _didx):
         (idx,) = ctx.saved_tensors
         return maxk_backward_scatter(dvals.contiguous(), idx, ctx.M), None
+
+
+def _need_1d(t: torch.Tensor, name: str, dtype) -> None:
+    if not (t.is_cuda or t.is_pinned()) or t.dim() != 1 or not t.is_contiguous() or t.dtype != dtype:
+        raise ValueError(f"{name} must be a contiguous 1-D {dtype} tensor on the GPU (or pinned)")
+
+
+def maxk_spgemm_forward(row_ptr: torch.Tensor, col_idx: torch.Tensor, edge_w: Optional[torch.Tensor],
+                        sp_data: torch.Tensor, sp_index: torch.Tensor, M: int, *,
+                        out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """MaxK-GNN forward aggregation: dense fp32 (n_dst x M) = graph (CSR over
+    destination rows) times the CBSR feature rows (bf16 sp_data, int16 sp_index)."""
+    _need_1d(row_ptr, "row_ptr", torch.int64)
+    _need_1d(col_idx, "col_idx", torch.int32)
+    if edge_w is not None:
+        _need_1d(edge_w, "edge_w", torch.float32)
+    _need_cuda_2d(sp_data, "sp_data")
+    _need_cuda_2d(sp_index, "sp_index")
+    if sp_data.dtype != torch.bfloat16 or sp_index.dtype != torch.int16 or sp_data.shape != sp_index.shape:
+        raise ValueError("sp_data must be bf16 and sp_index int16, both n_src x k")
+    n_dst = row_ptr.numel() - 1
+    n_src, k = sp_data.shape
+    if out is None:
+        out = _empty_like_home((n_dst, M), torch.float32, sp_data)
+    rc = _lib.load().maxk_spgemm_forward(row_ptr.data_ptr(), col_idx.data_ptr(), _ptr(edge_w), n_dst, n_src,
+                                         sp_data.data_ptr(), sp_index.data_ptr(), int(M), int(k), out.data_ptr(),
+                                         _ptr(status), _stream_ptr(stream, sp_data.device))
+    _lib.check(rc, "maxk_spgemm_forward")
+    return out
+
+
+def maxk_sspmm_backward(t_row_ptr: torch.Tensor, t_dst: torch.Tensor, t_edge_w: Optional[torch.Tensor],
+                        dout: torch.Tensor, sp_index: torch.Tensor, *, d_sp: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """MaxK-GNN backward of the aggregation: fp32 gradient of the CBSR values
+    (n_src x k), sampled at the forward sp_index. The graph is given transposed
+    (CSR over source rows: offsets, destination of each edge, edge weights)."""
+    _need_1d(t_row_ptr, "t_row_ptr", torch.int64)
+    _need_1d(t_dst, "t_dst", torch.int32)
+    if t_edge_w is not None:
+        _need_1d(t_edge_w, "t_edge_w", torch.float32)
+    _need_cuda_2d(dout, "dout")
+    _need_cuda_2d(sp_index, "sp_index")
+    if dout.dtype != torch.float32 or sp_index.dtype != torch.int16:
+        raise ValueError("dout must be float32 and sp_index int16")
+    n_dst, M = dout.shape
+    n_src, k = sp_index.shape
+    if t_row_ptr.numel() != n_src + 1:
+        raise ValueError("t_row_ptr must have n_src + 1 entries")
+    if d_sp is None:
+        d_sp = _empty_like_home((n_src, k), torch.float32, dout)
+    rc = _lib.load().maxk_sspmm_backward(t_row_ptr.data_ptr(), t_dst.data_ptr(), _ptr(t_edge_w), n_src, n_dst,
+                                         dout.data_ptr(), sp_index.data_ptr(), int(M), int(k), d_sp.data_ptr(),
+                                         _ptr(status), _stream_ptr(stream, dout.device))
+    _lib.check(rc, "maxk_sspmm_backward")
+    return d_sp

@@ -27,6 +27,14 @@ cudaError_t launch_select_bf16(const SelectArgs& a, bool idx16, cudaStream_t s);
 cudaError_t launch_maxk_backward(const uint16_t* dy, const int16_t* idx, int64_t N, int M, int k,
                                  uint16_t* grad, uint32_t* status, cudaStream_t s);
 
+// MaxK-GNN aggregation over CBSR (forward SpGEMM, backward sampled product).
+cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const float* w, int64_t n_dst,
+                              int64_t n_src, const uint16_t* sp_data, const int16_t* sp_index, int M, int k,
+                              float* out, uint32_t* status, cudaStream_t s);
+cudaError_t launch_sspmm_bwd(const int64_t* t_ptr, const int32_t* t_row, const float* t_w, int64_t n_src,
+                             int64_t n_dst, const float* dout, const int16_t* sp_index, int M, int k,
+                             float* d_sp, uint32_t* status, cudaStream_t s);
+
 // Persistent-grid size for `kernel` launched with `threads` threads per block:
 // SM count x resident blocks per SM (cached per device and kernel), capped at
 // the number of blocks the work needs.

@@ -10,6 +10,7 @@ struct Entry {
   int device;
   const void* kernel;
   int threads;
+  size_t smem;
   int blocks;
 };
 constexpr int kMaxEntries = 256;
@@ -26,7 +27,8 @@ int persistent_blocks(const void* kernel, int threads, size_t smem, int64_t bloc
   {
     std::lock_guard<std::mutex> lock(g_mu);
     for (int i = 0; i < g_used; ++i) {
-      if (g_cache[i].device == dev && g_cache[i].kernel == kernel && g_cache[i].threads == threads) {
+      if (g_cache[i].device == dev && g_cache[i].kernel == kernel && g_cache[i].threads == threads &&
+          g_cache[i].smem == smem) {
         per_gpu = g_cache[i].blocks;
         break;
       }
@@ -39,7 +41,7 @@ int persistent_blocks(const void* kernel, int threads, size_t smem, int64_t bloc
       return 0;
     per_gpu = sms * (occ > 0 ? occ : 1);
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_used < kMaxEntries) g_cache[g_used++] = Entry{dev, kernel, threads, per_gpu};
+    if (g_used < kMaxEntries) g_cache[g_used++] = Entry{dev, kernel, threads, smem, per_gpu};
   }
   if (blocks_needed < 1) blocks_needed = 1;
   return int(blocks_needed < per_gpu ? blocks_needed : per_gpu);

@@ -1,0 +1,231 @@
+// MaxK-GNN feature aggregation over CBSR, forward and backward, sm_103a.
+//
+// Source: "MaxK-GNN: Extremely Fast GPU Kernel Design for Accelerating Graph
+// Neural Networks Training", "How MaxK-GNN works" (forward: row-wise-product
+// SpGEMM over the compressed rows with shared-memory accumulation and one
+// global write per row; backward: a sampled product whose output positions are
+// the forward sp_index) and "Why it works" (each neighbour read shrinks from M
+// to k values; scatter-accumulation stays on chip).
+//
+// Forward  out[i, m] = sum over the edges e of destination row i, in edge
+//          order, of w_e * v for the CBSR entries (v, m) of source row col[e].
+// Backward d_sp[j, t] = sum over the edges e of source row j (transposed
+//          graph), in order, of w_e * dout[dst_e, sp_index[j, t]].
+//
+// Both kernels add in edge order with one rounding per product and per sum
+// (__fmul_rn / __fadd_rn), so results are deterministic and bit-identical to
+// the sequential binary32 definition. Forward: one warp per destination row
+// with an M-float accumulator in shared memory; a source row's k indices are
+// distinct, so the lanes of one edge never touch the same column and a
+// __syncwarp between edges orders the updates. Edge lists are read 32 at a
+// time (coalesced) and the CBSR rows of U edges are loaded before they are
+// applied, so U gathers are in flight per warp. Backward: one warp per source
+// row, lane t owns entry t, and the gathers of U edges are issued together.
+#include <cstdint>
+
+#include "launch.h"
+
+namespace rtopk {
+namespace {
+
+constexpr uint32_t kStatusBadIndex = 0x8u;
+constexpr uint32_t kStatusBadEdge = 0x10u;
+constexpr int kThreads = 256;
+constexpr int kU = 4;  // edges whose rows are in flight together
+
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+template <int KS>  // ceil(k / 32) entries per lane
+__global__ void __launch_bounds__(kThreads)
+spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                  const float* __restrict__ w, int64_t n_dst, int64_t n_src, const uint16_t* __restrict__ sp_data,
+                  const int16_t* __restrict__ sp_index, int M, int k, bool vec, float* __restrict__ out,
+                  uint32_t* __restrict__ status) {
+  extern __shared__ __align__(16) float acc_all[];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  float* acc = acc_all + size_t(wib) * M;
+  const int64_t nw = int64_t(gridDim.x) * wpb;
+  uint32_t st = 0;
+  for (int64_t i = int64_t(blockIdx.x) * wpb + wib; i < n_dst; i += nw) {
+    if (vec) {
+      for (int m = lane * 4; m < M; m += 128) *reinterpret_cast<float4*>(acc + m) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int m = lane; m < M; m += 32) acc[m] = 0.0f;
+    }
+    __syncwarp();
+    const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+    for (int64_t c0 = e0; c0 < e1; c0 += 32) {
+      const int nc = (e1 - c0 < 32) ? int(e1 - c0) : 32;
+      const int32_t cj = (lane < nc) ? col[c0 + lane] : 0;
+      const float cw = (lane < nc) ? (w != nullptr ? w[c0 + lane] : 1.0f) : 0.0f;
+      for (int u = 0; u < nc; u += kU) {
+        float v[kU][KS];
+        int c[kU][KS];
+        float we[kU];
+        bool okj[kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+          const int64_t j = __shfl_sync(0xffffffffu, cj, (u + q) & 31);
+          we[q] = __shfl_sync(0xffffffffu, cw, (u + q) & 31);
+          okj[q] = (u + q < nc) && j >= 0 && j < n_src;
+          if (u + q < nc && !okj[q]) st |= kStatusBadEdge;
+#pragma unroll
+          for (int s = 0; s < KS; ++s) {
+            const int t = s * 32 + lane;
+            if (okj[q] && t < k) {
+              v[q][s] = bf16f(sp_data[j * k + t]);
+              c[q][s] = sp_index[j * k + t];
+            } else {
+              v[q][s] = 0.0f;
+              c[q][s] = -1;
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+#pragma unroll
+          for (int s = 0; s < KS; ++s) {
+            const int t = s * 32 + lane;
+            if (okj[q] && t < k) {
+              const int m = c[q][s];
+              if (m >= 0 && m < M) {
+                acc[m] = __fadd_rn(acc[m], __fmul_rn(we[q], v[q][s]));
+              } else {
+                st |= kStatusBadIndex;
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
+    }
+    float* o = out + i * int64_t(M);
+    if (vec) {
+      for (int m = lane * 4; m < M; m += 128) __stcs(reinterpret_cast<float4*>(o + m), *reinterpret_cast<const float4*>(acc + m));
+    } else {
+      for (int m = lane; m < M; m += 32) __stcs(o + m, acc[m]);
+    }
+    __syncwarp();
+  }
+  if (status != nullptr && st != 0u) atomicOr(status, st);
+}
+
+template <int KS>
+__global__ void __launch_bounds__(kThreads)
+sspmm_bwd_kernel(const int64_t* __restrict__ t_ptr, const int32_t* __restrict__ t_row,
+                 const float* __restrict__ t_w, int64_t n_src, int64_t n_dst, const float* __restrict__ dout,
+                 const int16_t* __restrict__ sp_index, int M, int k, float* __restrict__ d_sp,
+                 uint32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  const int64_t nw = int64_t(gridDim.x) * wpb;
+  uint32_t st = 0;
+  for (int64_t j = int64_t(blockIdx.x) * wpb + wib; j < n_src; j += nw) {
+    int c[KS];
+    float acc[KS];
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      const int t = s * 32 + lane;
+      c[s] = (t < k) ? sp_index[j * k + t] : 0;
+      if (t < k && (c[s] < 0 || c[s] >= M)) { st |= kStatusBadIndex; c[s] = -1; }
+      acc[s] = 0.0f;
+    }
+    const int64_t e0 = t_ptr[j], e1 = t_ptr[j + 1];
+    for (int64_t c0 = e0; c0 < e1; c0 += 32) {
+      const int nc = (e1 - c0 < 32) ? int(e1 - c0) : 32;
+      const int32_t ci = (lane < nc) ? t_row[c0 + lane] : 0;
+      const float cw = (lane < nc) ? (t_w != nullptr ? t_w[c0 + lane] : 1.0f) : 0.0f;
+      for (int u = 0; u < nc; u += kU) {
+        float g[kU][KS], we[kU];
+        bool oki[kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+          const int64_t i = __shfl_sync(0xffffffffu, ci, (u + q) & 31);
+          we[q] = __shfl_sync(0xffffffffu, cw, (u + q) & 31);
+          oki[q] = (u + q < nc) && i >= 0 && i < n_dst;
+          if (u + q < nc && !oki[q]) st |= kStatusBadEdge;
+#pragma unroll
+          for (int s = 0; s < KS; ++s) {
+            const int t = s * 32 + lane;
+            g[q][s] = (oki[q] && t < k && c[s] >= 0) ? __ldg(dout + i * int64_t(M) + c[s]) : 0.0f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q)
+#pragma unroll
+          for (int s = 0; s < KS; ++s)
+            if (oki[q]) acc[s] = __fadd_rn(acc[s], __fmul_rn(we[q], g[q][s]));
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+      const int t = s * 32 + lane;
+      if (t < k) d_sp[j * k + t] = acc[s];
+    }
+  }
+  if (status != nullptr && st != 0u) atomicOr(status, st);
+}
+
+template <typename Kern>
+cudaError_t launch_rows(Kern kern, int64_t rows, size_t smem_per_warp, cudaStream_t s, int& threads, int& blocks) {
+  // warps per block limited by the shared accumulator (48 KB without opt-in)
+  int wpb = kThreads / 32;
+  if (smem_per_warp > 0) {
+    const int fit = int((48 * 1024) / smem_per_warp);
+    wpb = fit < wpb ? (fit < 1 ? 1 : fit) : wpb;
+  }
+  threads = wpb * 32;
+  blocks = persistent_blocks(reinterpret_cast<const void*>(kern), threads, smem_per_warp * wpb,
+                             (rows + wpb - 1) / wpb);
+  return blocks > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+}  // namespace
+
+cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const float* w, int64_t n_dst,
+                              int64_t n_src, const uint16_t* sp_data, const int16_t* sp_index, int M, int k,
+                              float* out, uint32_t* status, cudaStream_t s) {
+  const int ks = (k + 31) / 32;
+  const size_t smem_warp = size_t(M) * sizeof(float);
+  // 16-byte accumulator and output rows need M % 4 == 0 and an aligned output
+  const bool vec = (M % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0);
+  int threads = 0, blocks = 0;
+#define RTOPK_FWD(KS)                                                                                     \
+  {                                                                                                       \
+    cudaError_t e = launch_rows(spgemm_fwd_kernel<KS>, n_dst, smem_warp, s, threads, blocks);             \
+    if (e != cudaSuccess) return e;                                                                       \
+    spgemm_fwd_kernel<KS><<<blocks, threads, smem_warp * (threads / 32), s>>>(                            \
+        row_ptr, col, w, n_dst, n_src, sp_data, sp_index, M, k, vec, out, status);                             \
+    return cudaGetLastError();                                                                            \
+  }
+  if (ks <= 1) RTOPK_FWD(1)
+  if (ks <= 2) RTOPK_FWD(2)
+  if (ks <= 4) RTOPK_FWD(4)
+  RTOPK_FWD(8)
+#undef RTOPK_FWD
+}
+
+cudaError_t launch_sspmm_bwd(const int64_t* t_ptr, const int32_t* t_row, const float* t_w, int64_t n_src,
+                             int64_t n_dst, const float* dout, const int16_t* sp_index, int M, int k,
+                             float* d_sp, uint32_t* status, cudaStream_t s) {
+  const int ks = (k + 31) / 32;
+  int threads = 0, blocks = 0;
+#define RTOPK_BWD(KS)                                                                                     \
+  {                                                                                                       \
+    cudaError_t e = launch_rows(sspmm_bwd_kernel<KS>, n_src, 0, s, threads, blocks);                      \
+    if (e != cudaSuccess) return e;                                                                       \
+    sspmm_bwd_kernel<KS><<<blocks, threads, 0, s>>>(t_ptr, t_row, t_w, n_src, n_dst, dout, sp_index, M, k, \
+                                                     d_sp, status);                                       \
+    return cudaGetLastError();                                                                            \
+  }
+  if (ks <= 1) RTOPK_BWD(1)
+  if (ks <= 2) RTOPK_BWD(2)
+  if (ks <= 4) RTOPK_BWD(4)
+  RTOPK_BWD(8)
+#undef RTOPK_BWD
+}
+
+}  // namespace rtopk

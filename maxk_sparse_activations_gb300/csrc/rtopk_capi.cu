@@ -55,6 +55,33 @@ int maxk_backward_scatter(const void* dy_bf16, const int16_t* idx, int64_t N, in
                                                static_cast<uint16_t*>(grad_bf16), status, stream));
 }
 
+int maxk_spgemm_forward(const int64_t* row_ptr, const int32_t* col_idx, const float* edge_w, int64_t n_dst,
+                        int64_t n_src, const void* sp_data_bf16, const int16_t* sp_index, int32_t M, int32_t k,
+                        float* out, uint32_t* status, cudaStream_t stream) {
+  if (n_dst < 0 || n_src < 0 || M < 1 || M > RTOPK_MAX_M) return RTOPK_EINVAL_SHAPE;
+  if (k < 1 || k > M || k > RTOPK_GNN_MAX_K) return RTOPK_EINVAL_K;
+  if (n_dst > 0 && (row_ptr == nullptr || out == nullptr || (n_src > 0 && (col_idx == nullptr ||
+                    sp_data_bf16 == nullptr || sp_index == nullptr))))
+    return RTOPK_EINVAL_PTR;
+  if (n_dst == 0) return RTOPK_OK;
+  return from_cuda(rtopk::launch_spgemm_fwd(row_ptr, col_idx, edge_w, n_dst, n_src,
+                                            static_cast<const uint16_t*>(sp_data_bf16), sp_index, M, k, out,
+                                            status, stream));
+}
+
+int maxk_sspmm_backward(const int64_t* t_row_ptr, const int32_t* t_dst, const float* t_edge_w, int64_t n_src,
+                        int64_t n_dst, const float* dout, const int16_t* sp_index, int32_t M, int32_t k,
+                        float* d_sp_data, uint32_t* status, cudaStream_t stream) {
+  if (n_dst < 0 || n_src < 0 || M < 1 || M > RTOPK_MAX_M) return RTOPK_EINVAL_SHAPE;
+  if (k < 1 || k > M || k > RTOPK_GNN_MAX_K) return RTOPK_EINVAL_K;
+  if (n_src > 0 && (t_row_ptr == nullptr || sp_index == nullptr || d_sp_data == nullptr ||
+                    (n_dst > 0 && (t_dst == nullptr || dout == nullptr))))
+    return RTOPK_EINVAL_PTR;
+  if (n_src == 0) return RTOPK_OK;
+  return from_cuda(rtopk::launch_sspmm_bwd(t_row_ptr, t_dst, t_edge_w, n_src, n_dst, dout, sp_index, M, k,
+                                           d_sp_data, status, stream));
+}
+
 const char* rtopk_strerror(int code) {
   switch (code) {
     case RTOPK_OK: return "ok";

@@ -20,7 +20,7 @@ import numpy as np
 __all__ = [
     "normal_f32", "uniform_pm1_f32", "int_ties_f32", "all_equal_rows_f32",
     "outliers_f32", "subnormals_f32", "f32_to_bf16_bits", "normal_bf16",
-    "make", "VALUE_SETS",
+    "make", "VALUE_SETS", "power_law_graph", "transpose_graph",
 ]
 
 
@@ -101,3 +101,37 @@ def make(value_set: str, N: int, M: int, seed: int = 0, dtype: str = "f32") -> n
     if dtype == "bf16":
         return f32_to_bf16_bits(x)
     raise ValueError(dtype)
+
+
+def power_law_graph(n_dst: int, n_src: int, avg_degree: float, seed: int = 0, alpha: float = 2.2,
+                    max_degree: int | None = None):
+    """Synthetic GNN graph in CSR over destination rows (stand-in for the pages'
+    Reddit / Flickr / Ogbn-products / Yelp graphs, which are not available).
+
+    In-degrees follow a Pareto tail with exponent ``alpha`` scaled to the mean
+    ``avg_degree`` (at least 1, at most ``max_degree`` or ``n_src``); sources
+    are uniform. Edge weights are 1 / in-degree (mean aggregation).
+    Returns (row_ptr int64 [n_dst + 1], col int32 [E], w float32 [E]).
+    """
+    g = _rng(seed)
+    raw = g.pareto(alpha - 1.0, size=n_dst) + 1.0
+    deg = np.maximum(1, np.rint(raw * (avg_degree / raw.mean()))).astype(np.int64)
+    deg = np.minimum(deg, max_degree if max_degree is not None else n_src)
+    row_ptr = np.zeros(n_dst + 1, dtype=np.int64)
+    np.cumsum(deg, out=row_ptr[1:])
+    col = g.integers(0, n_src, size=int(row_ptr[-1]), dtype=np.int64).astype(np.int32)
+    w = np.repeat((1.0 / deg).astype(np.float32), deg)
+    return row_ptr, col, w
+
+
+def transpose_graph(row_ptr, col, w, n_src: int):
+    """The same edges grouped by source row: (t_ptr int64 [n_src + 1],
+    t_row int32 [E] = destination of each edge, t_w float32 [E]). Within a source
+    the edges keep their forward order (ascending destination)."""
+    row_ptr = np.asarray(row_ptr, dtype=np.int64)
+    n_dst = row_ptr.shape[0] - 1
+    dst = np.repeat(np.arange(n_dst, dtype=np.int32), np.diff(row_ptr))
+    order = np.argsort(np.asarray(col), kind="stable")
+    t_ptr = np.zeros(n_src + 1, dtype=np.int64)
+    np.cumsum(np.bincount(np.asarray(col), minlength=n_src), out=t_ptr[1:])
+    return t_ptr, np.ascontiguousarray(dst[order]), np.ascontiguousarray(np.asarray(w, dtype=np.float32)[order])

@@ -22,6 +22,13 @@ Functions (each follows the page and section named in ``rtopk_oracle.c``):
 * ``maxk_backward(dy, idx, M)`` -- the MaxK backward scatter: the gradient row
   is zero except at the kept positions. ("MaxK-GNN ...", "How MaxK-GNN works",
   "Asymmetric passes, one mask".)
+* ``spgemm_cbsr(graph, sp_data, sp_index, M)`` -- MaxK-GNN forward aggregation:
+  each destination row sums its neighbours' CBSR rows, scattered to their
+  columns, in edge order (binary32, no FMA). ("MaxK-GNN ...", "How MaxK-GNN
+  works", "Why it works".)
+* ``sspmm_cbsr(tgraph, dout, sp_index, n_dst)`` -- the backward sampled product:
+  the gradient of each CBSR value sums, over the source row's out-edges in
+  order, the edge weight times dout at (destination, sp_index).
 
 bf16 inputs are widened exactly to binary32 (the 16 bits become the top half of
 the word) and run through the same functions; kept values are the original
@@ -67,8 +74,10 @@ def _load():
             lib.oracle_brute_topk.argtypes = [p, i64, i32, i32, p]
             lib.oracle_replay.argtypes = [p, i64, i32, i32, i32, f32, p, p]
             lib.oracle_maxk_backward_u16.argtypes = [p, p, i64, i32, i32, p]
+            lib.oracle_spgemm_cbsr.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p]
+            lib.oracle_sspmm_cbsr.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p]
             for f in (lib.oracle_sort_topk, lib.oracle_brute_topk, lib.oracle_replay,
-                      lib.oracle_maxk_backward_u16):
+                      lib.oracle_maxk_backward_u16, lib.oracle_spgemm_cbsr, lib.oracle_sspmm_cbsr):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -143,3 +152,35 @@ def maxk_backward(dy_bits: np.ndarray, idx: np.ndarray, M: int) -> np.ndarray:
     _check(_load().oracle_maxk_backward_u16(_ptr(dy), _ptr(ix), N, M, k, _ptr(grad)),
            "maxk_backward")
     return grad
+
+
+def spgemm_cbsr(row_ptr, col, w, n_src: int, sp_data_bits, sp_index, M: int) -> np.ndarray:
+    """Forward aggregation over CBSR: dense (n_dst x M) float32."""
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    cl = np.ascontiguousarray(col, dtype=np.int32)
+    wt = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    sd = np.ascontiguousarray(sp_data_bits, dtype=np.uint16)
+    si = np.ascontiguousarray(sp_index, dtype=np.int16)
+    n_dst = rp.shape[0] - 1
+    k = sd.shape[1]
+    out = np.empty((n_dst, M), dtype=np.float32)
+    rc = _load().oracle_spgemm_cbsr(_ptr(rp), _ptr(cl), None if wt is None else _ptr(wt), n_dst, n_src,
+                                    _ptr(sd), _ptr(si), M, k, _ptr(out))
+    _check(rc, "spgemm_cbsr")
+    return out
+
+
+def sspmm_cbsr(t_ptr, t_row, t_w, n_dst: int, dout, sp_index) -> np.ndarray:
+    """Backward sampled product: float32 (n_src x k) gradient of the CBSR values."""
+    tp = np.ascontiguousarray(t_ptr, dtype=np.int64)
+    tr = np.ascontiguousarray(t_row, dtype=np.int32)
+    tw = None if t_w is None else np.ascontiguousarray(t_w, dtype=np.float32)
+    do = np.ascontiguousarray(dout, dtype=np.float32)
+    si = np.ascontiguousarray(sp_index, dtype=np.int16)
+    n_src, k = si.shape
+    M = do.shape[1]
+    out = np.empty((n_src, k), dtype=np.float32)
+    rc = _load().oracle_sspmm_cbsr(_ptr(tp), _ptr(tr), None if tw is None else _ptr(tw), n_src, n_dst,
+                                   _ptr(do), _ptr(si), M, k, _ptr(out))
+    _check(rc, "sspmm_cbsr")
+    return out

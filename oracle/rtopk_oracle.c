@@ -245,3 +245,71 @@ int oracle_maxk_backward_u16(const uint16_t* dy, const int16_t* idx, int64_t N, 
   }
   return ORACLE_OK;
 }
+
+/* --------------------------------------------------------------------- */
+/* MaxK-GNN aggregation over CBSR ([MaxK] "How MaxK-GNN works": forward    */
+/* feature aggregation as a row-wise-product SpGEMM over the compressed    */
+/* rows; "Asymmetric passes, one mask" and "Why it works": the backward   */
+/* pass is a sampled product evaluated only at the forward sp_index).     */
+/*                                                                         */
+/* Forward: out[i, m] = sum over the edges e of destination row i, in      */
+/* edge order, of w_e * v, where (v, m) runs over the CBSR entries          */
+/* (value, index) of source row col[e]; w_e = 1 when no weights are given.  */
+/* binary32: each product and each running sum rounded, no FMA, starting   */
+/* from +0. A source row's indices are distinct, so each out[i, m] gets at */
+/* most one term per edge and the order of terms is the edge order.        */
+/* --------------------------------------------------------------------- */
+
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+int oracle_spgemm_cbsr(const int64_t* row_ptr, const int32_t* col, const float* w, int64_t n_dst,
+                       int64_t n_src, const uint16_t* sp_data, const int16_t* sp_index, int32_t M,
+                       int32_t k, float* out) {
+  if (n_dst < 0 || n_src < 0 || M < 1 || k < 1 || k > M) return ORACLE_EARG;
+  for (int64_t i = 0; i < n_dst; ++i) {
+    float* o = out + i * (int64_t)M;
+    for (int32_t m = 0; m < M; ++m) o[m] = 0.0f;
+    for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) {
+      const int64_t j = col[e];
+      if (j < 0 || j >= n_src) return ORACLE_EINPUT;
+      const float we = w ? w[e] : 1.0f;
+      for (int32_t t = 0; t < k; ++t) {
+        const int32_t m = sp_index[j * k + t];
+        if (m < 0 || m >= M) return ORACLE_EINPUT;
+        const float p = we * bf16_to_f32(sp_data[j * k + t]);
+        o[m] = o[m] + p;
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* Backward: d_sp[j, t] = sum over the edges e of source row j in the     */
+/* transposed graph (destination t_row[e], weight t_w[e]), in that order,   */
+/* of w_e * dout[t_row[e], sp_index[j, t]]. binary32, no FMA, from +0.     */
+int oracle_sspmm_cbsr(const int64_t* t_ptr, const int32_t* t_row, const float* t_w, int64_t n_src,
+                      int64_t n_dst, const float* dout, const int16_t* sp_index, int32_t M, int32_t k,
+                      float* d_sp) {
+  if (n_dst < 0 || n_src < 0 || M < 1 || k < 1 || k > M) return ORACLE_EARG;
+  for (int64_t j = 0; j < n_src; ++j) {
+    for (int32_t t = 0; t < k; ++t) {
+      const int32_t m = sp_index[j * k + t];
+      if (m < 0 || m >= M) return ORACLE_EINPUT;
+      float acc = 0.0f;
+      for (int64_t e = t_ptr[j]; e < t_ptr[j + 1]; ++e) {
+        const int64_t i = t_row[e];
+        if (i < 0 || i >= n_dst) return ORACLE_EINPUT;
+        const float we = t_w ? t_w[e] : 1.0f;
+        const float p = we * dout[i * (int64_t)M + m];
+        acc = acc + p;
+      }
+      d_sp[j * k + t] = acc;
+    }
+  }
+  return ORACLE_OK;
+}

@@ -62,3 +62,13 @@ def test_argument_errors_launch_nothing(lib):
     assert lib.maxk_backward_scatter(None, None, 5, 8, 2, None, None, None) == -3
     assert lib.maxk_backward_scatter(None, None, 5, 9000, 2, None, None, None) == -1
     assert lib.maxk_backward_scatter(None, None, 0, 8, 2, None, None, None) == 0
+    F = lib.maxk_spgemm_forward
+    assert F(None, None, None, -1, 4, None, None, 8, 2, None, None, None) == -1   # n_dst < 0
+    assert F(None, None, None, 4, 4, None, None, 8, 9, None, None, None) == -2    # k > M
+    assert F(None, None, None, 4, 4, None, None, 512, 300, None, None, None) == -2  # k > 256
+    assert F(None, None, None, 4, 4, None, None, 8, 2, None, None, None) == -3    # NULL pointers
+    assert F(None, None, None, 0, 4, None, None, 8, 2, None, None, None) == 0     # no rows
+    B = lib.maxk_sspmm_backward
+    assert B(None, None, None, 4, 4, None, None, 9000, 2, None, None, None) == -1  # M > 8192
+    assert B(None, None, None, 4, 4, None, None, 8, 2, None, None, None) == -3
+    assert B(None, None, None, 0, 4, None, None, 8, 2, None, None, None) == 0
