@@ -154,7 +154,11 @@ int maxk_backward_scatter(const void* dy_bf16, const int16_t* idx, int64_t N, in
  *  out[i, m] = sum over the edges e of destination row i, in edge order, of
  *              edge_w[e] * v for every CBSR entry (v, m) of source row
  *              col_idx[e]; binary32 products and sums, one rounding each, no
- *              FMA -- results are deterministic and order-exact.
+ *              FMA -- deterministic, and bit-identical to that sequential sum
+ *              for rows of at most 512 edges. Longer rows are split into
+ *              chunks of 512 edges summed by the warps of one block and then
+ *              combined in a fixed order: still deterministic, and within
+ *              2 (deg + 1) 2^-24 sum|terms| of the sequential sum.
  *
  *  row_ptr      device, n_dst + 1 int64: CSR offsets over destination rows
  *  col_idx      device, E int32: source row of each edge (0 <= j < n_src)

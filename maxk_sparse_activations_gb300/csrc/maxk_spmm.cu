@@ -14,12 +14,16 @@
 //
 // Both kernels add in edge order with one rounding per product and per sum
 // (__fmul_rn / __fadd_rn), so results are deterministic and bit-identical to
-// the sequential binary32 definition. Forward: one warp per destination row
+// the sequential binary32 definition -- except forward rows with more than
+// 512 edges, which are summed in chunks (deterministic, within the binary32
+// bound of the sequential sum). Forward: one warp per destination row
 // with an M-float accumulator in shared memory; a source row's k indices are
 // distinct, so the lanes of one edge never touch the same column and a
 // __syncwarp between edges orders the updates. Edge lists are read 32 at a
 // time (coalesced) and the CBSR rows of U edges are loaded before they are
-// applied, so U gathers are in flight per warp. Backward: one warp per source
+// applied, so U gathers are in flight per warp. Rows with more than 512 edges
+// (the heavy tail of power-law graphs) go to a second kernel that spreads
+// each such row over the warps of one block. Backward: one warp per source
 // row, lane t owns entry t, and the gathers of U edges are issued together.
 #include <cstdint>
 
@@ -32,15 +36,81 @@ constexpr uint32_t kStatusBadIndex = 0x8u;
 constexpr uint32_t kStatusBadEdge = 0x10u;
 constexpr int kThreads = 256;
 constexpr int kU = 4;  // edges whose rows are in flight together
+// Rows with more edges than this are split over the warps of one block.
+constexpr int64_t kHeavyEdges = 512;
 
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
-template <int KS>  // ceil(k / 32) entries per lane
+// Adds the edges [e0, e1) of one destination row into the warp's shared
+// accumulator, in edge order (binary32, one rounding per product and sum).
+template <int KS>
+__device__ __forceinline__ void accumulate_edges(float* __restrict__ acc, const int32_t* __restrict__ col,
+                                                 const float* __restrict__ w, int64_t e0, int64_t e1,
+                                                 int64_t n_src, const uint16_t* __restrict__ sp_data,
+                                                 const int16_t* __restrict__ sp_index, int M, int k, int lane,
+                                                 uint32_t& st) {
+  for (int64_t c0 = e0; c0 < e1; c0 += 32) {
+    const int nc = (e1 - c0 < 32) ? int(e1 - c0) : 32;
+    const int32_t cj = (lane < nc) ? col[c0 + lane] : 0;
+    const float cw = (lane < nc) ? (w != nullptr ? w[c0 + lane] : 1.0f) : 0.0f;
+    for (int u = 0; u < nc; u += kU) {
+      float v[kU][KS];
+      int c[kU][KS];
+      float we[kU];
+      bool okj[kU];
+#pragma unroll
+      for (int q = 0; q < kU; ++q) {
+        const int64_t j = __shfl_sync(0xffffffffu, cj, (u + q) & 31);
+        we[q] = __shfl_sync(0xffffffffu, cw, (u + q) & 31);
+        okj[q] = (u + q < nc) && j >= 0 && j < n_src;
+        if (u + q < nc && !okj[q]) st |= kStatusBadEdge;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          const int t = s * 32 + lane;
+          if (okj[q] && t < k) {
+            v[q][s] = bf16f(sp_data[j * k + t]);
+            c[q][s] = sp_index[j * k + t];
+          } else {
+            v[q][s] = 0.0f;
+            c[q][s] = -1;
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kU; ++q) {
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          const int t = s * 32 + lane;
+          if (okj[q] && t < k) {
+            const int m = c[q][s];
+            if (m >= 0 && m < M) {
+              acc[m] = __fadd_rn(acc[m], __fmul_rn(we[q], v[q][s]));
+            } else {
+              st |= kStatusBadIndex;
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void zero_row(float* __restrict__ acc, int M, int lane, bool vec) {
+  if (vec) {
+    for (int m = lane * 4; m < M; m += 128) *reinterpret_cast<float4*>(acc + m) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    for (int m = lane; m < M; m += 32) acc[m] = 0.0f;
+  }
+}
+
+// Destination rows with at most `heavy` edges: one warp per row, edges in order.
+template <int KS>
 __global__ void __launch_bounds__(kThreads)
 spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
                   const float* __restrict__ w, int64_t n_dst, int64_t n_src, const uint16_t* __restrict__ sp_data,
-                  const int16_t* __restrict__ sp_index, int M, int k, bool vec, float* __restrict__ out,
-                  uint32_t* __restrict__ status) {
+                  const int16_t* __restrict__ sp_index, int M, int k, int64_t heavy, bool vec,
+                  float* __restrict__ out, uint32_t* __restrict__ status) {
   extern __shared__ __align__(16) float acc_all[];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
@@ -49,58 +119,11 @@ spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict
   const int64_t nw = int64_t(gridDim.x) * wpb;
   uint32_t st = 0;
   for (int64_t i = int64_t(blockIdx.x) * wpb + wib; i < n_dst; i += nw) {
-    if (vec) {
-      for (int m = lane * 4; m < M; m += 128) *reinterpret_cast<float4*>(acc + m) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      for (int m = lane; m < M; m += 32) acc[m] = 0.0f;
-    }
-    __syncwarp();
     const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
-    for (int64_t c0 = e0; c0 < e1; c0 += 32) {
-      const int nc = (e1 - c0 < 32) ? int(e1 - c0) : 32;
-      const int32_t cj = (lane < nc) ? col[c0 + lane] : 0;
-      const float cw = (lane < nc) ? (w != nullptr ? w[c0 + lane] : 1.0f) : 0.0f;
-      for (int u = 0; u < nc; u += kU) {
-        float v[kU][KS];
-        int c[kU][KS];
-        float we[kU];
-        bool okj[kU];
-#pragma unroll
-        for (int q = 0; q < kU; ++q) {
-          const int64_t j = __shfl_sync(0xffffffffu, cj, (u + q) & 31);
-          we[q] = __shfl_sync(0xffffffffu, cw, (u + q) & 31);
-          okj[q] = (u + q < nc) && j >= 0 && j < n_src;
-          if (u + q < nc && !okj[q]) st |= kStatusBadEdge;
-#pragma unroll
-          for (int s = 0; s < KS; ++s) {
-            const int t = s * 32 + lane;
-            if (okj[q] && t < k) {
-              v[q][s] = bf16f(sp_data[j * k + t]);
-              c[q][s] = sp_index[j * k + t];
-            } else {
-              v[q][s] = 0.0f;
-              c[q][s] = -1;
-            }
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < kU; ++q) {
-#pragma unroll
-          for (int s = 0; s < KS; ++s) {
-            const int t = s * 32 + lane;
-            if (okj[q] && t < k) {
-              const int m = c[q][s];
-              if (m >= 0 && m < M) {
-                acc[m] = __fadd_rn(acc[m], __fmul_rn(we[q], v[q][s]));
-              } else {
-                st |= kStatusBadIndex;
-              }
-            }
-          }
-          __syncwarp();
-        }
-      }
-    }
+    if (e1 - e0 > heavy) continue;  // left to spgemm_heavy_kernel
+    zero_row(acc, M, lane, vec);
+    __syncwarp();
+    accumulate_edges<KS>(acc, col, w, e0, e1, n_src, sp_data, sp_index, M, k, lane, st);
     float* o = out + i * int64_t(M);
     if (vec) {
       for (int m = lane * 4; m < M; m += 128) __stcs(reinterpret_cast<float4*>(o + m), *reinterpret_cast<const float4*>(acc + m));
@@ -108,6 +131,44 @@ spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict
       for (int m = lane; m < M; m += 32) __stcs(o + m, acc[m]);
     }
     __syncwarp();
+  }
+  if (status != nullptr && st != 0u) atomicOr(status, st);
+}
+
+// Destination rows with more than `heavy` edges: one block per row. Warp q
+// adds the edge chunks q, q + W, ... (chunks of `heavy` edges, each in edge
+// order) into its own accumulator; the W partial rows are then summed in warp
+// order. Deterministic, but the terms of such a row are not added in plain
+// edge order (the bound on the difference is in the C ABI header).
+template <int KS>
+__global__ void __launch_bounds__(kThreads)
+spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                    const float* __restrict__ w, int64_t n_dst, int64_t n_src,
+                    const uint16_t* __restrict__ sp_data, const int16_t* __restrict__ sp_index, int M, int k,
+                    int64_t heavy, bool vec, float* __restrict__ out, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(16) float acc_all[];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  float* acc = acc_all + size_t(wib) * M;
+  uint32_t st = 0;
+  for (int64_t i = blockIdx.x; i < n_dst; i += gridDim.x) {
+    const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
+    if (e1 - e0 <= heavy) continue;  // block-uniform
+    zero_row(acc, M, lane, vec);
+    __syncwarp();
+    for (int64_t c0 = e0 + int64_t(wib) * heavy; c0 < e1; c0 += int64_t(wpb) * heavy) {
+      const int64_t c1 = (e1 - c0 < heavy) ? e1 : c0 + heavy;
+      accumulate_edges<KS>(acc, col, w, c0, c1, n_src, sp_data, sp_index, M, k, lane, st);
+    }
+    __syncthreads();
+    float* o = out + i * int64_t(M);
+    for (int m = threadIdx.x; m < M; m += blockDim.x) {
+      float sum = acc_all[m];
+      for (int q = 1; q < wpb; ++q) sum = __fadd_rn(sum, acc_all[size_t(q) * M + m]);
+      __stcs(o + m, sum);
+    }
+    __syncthreads();
   }
   if (status != nullptr && st != 0u) atomicOr(status, st);
 }
@@ -198,7 +259,13 @@ cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const 
     cudaError_t e = launch_rows(spgemm_fwd_kernel<KS>, n_dst, smem_warp, s, threads, blocks);             \
     if (e != cudaSuccess) return e;                                                                       \
     spgemm_fwd_kernel<KS><<<blocks, threads, smem_warp * (threads / 32), s>>>(                            \
-        row_ptr, col, w, n_dst, n_src, sp_data, sp_index, M, k, vec, out, status);                             \
+        row_ptr, col, w, n_dst, n_src, sp_data, sp_index, M, k, kHeavyEdges, vec, out, status);           \
+    e = cudaGetLastError();                                                                               \
+    if (e != cudaSuccess) return e;                                                                       \
+    e = launch_rows(spgemm_heavy_kernel<KS>, n_dst * (threads / 32), smem_warp, s, threads, blocks);      \
+    if (e != cudaSuccess) return e;                                                                       \
+    spgemm_heavy_kernel<KS><<<blocks, threads, smem_warp * (threads / 32), s>>>(                          \
+        row_ptr, col, w, n_dst, n_src, sp_data, sp_index, M, k, kHeavyEdges, vec, out, status);           \
     return cudaGetLastError();                                                                            \
   }
   if (ks <= 1) RTOPK_FWD(1)

@@ -1,6 +1,7 @@
 """GPU parity of the MaxK-GNN aggregation over CBSR (forward SpGEMM, backward
 sampled product) against the oracle: bit-exact, since both add in edge order
-with one binary32 rounding per product and per sum. CBSR inputs come from the
+with one binary32 rounding per product and per sum (forward rows with more than
+512 edges are summed in chunks and compared within the binary32 bound). CBSR inputs come from the
 oracle's own selection, so no oracle input comes from the CUDA path.
 ("MaxK-GNN: Extremely Fast GPU Kernel Design for Accelerating Graph Neural
 Networks Training", "How MaxK-GNN works", "Asymmetric passes, one mask".)
@@ -49,7 +50,8 @@ def _run_fwd(row_ptr, col, w, sp_data, sp_index, M):
 def test_forward_bit_exact(M, k, weighted):
     n_src, n_dst = 3000, 2500
     sp_data, sp_index = _cbsr(n_src, M, k, seed=M + k)
-    row_ptr, col, w = synth.power_law_graph(n_dst, n_src, 16.0, seed=1)
+    # in-degree <= 512: every row takes the sequential single-warp path
+    row_ptr, col, w = synth.power_law_graph(n_dst, n_src, 16.0, seed=1, max_degree=512)
     w = w if weighted else None
     got, st = _run_fwd(row_ptr, col, w, sp_data, sp_index, M)
     want = oracle.spgemm_cbsr(row_ptr, col, w, n_src, sp_data, sp_index, M)
@@ -73,8 +75,20 @@ def test_forward_large_graph_and_empty_rows():
     got, st = _run_fwd(row_ptr2, col2, w2, sp_data, sp_index, M)
     want = oracle.spgemm_cbsr(row_ptr2, col2, w2, n_src, sp_data, sp_index, M)
     assert st == 0
-    np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))
     assert np.all(got[::97] == 0)
+    deg = np.diff(row_ptr2)
+    light = deg <= 512
+    assert (~light).sum() > 10  # the power-law tail exercises the chunked path
+    np.testing.assert_array_equal(got[light].view(np.uint32), want[light].view(np.uint32))
+    # chunked rows: both sums are within (deg + 1) 2^-24 sum|terms| of the exact sum
+    H = np.zeros((n_src, M))
+    vals = (sp_data.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    np.put_along_axis(H, sp_index.astype(np.int64), vals, axis=1)
+    for i in np.flatnonzero(~light):
+        e = slice(row_ptr2[i], row_ptr2[i + 1])
+        absref = np.abs(w2[e].astype(np.float64)) @ np.abs(H[col2[e]])
+        bound = 2 * (deg[i] + 1) * 2.0 ** -24 * absref * 1.0001
+        assert np.all(np.abs(got[i].astype(np.float64) - want[i]) <= bound), i
 
 
 @pytest.mark.parametrize("M,k", [(256, 32), (512, 64), (1024, 256), (100, 7)])
@@ -109,7 +123,7 @@ def test_fused_maxk_layer_chain():
     against the same chain on the oracle."""
     n, M, k = 4096, 256, 32
     xb = synth.normal_bf16(n, M, seed=31)
-    row_ptr, col, w = synth.power_law_graph(n, n, 24.0, seed=32)
+    row_ptr, col, w = synth.power_law_graph(n, n, 24.0, seed=32, max_degree=512)
     t_ptr, t_row, t_w = synth.transpose_graph(row_ptr, col, w, n)
     dout = synth.normal_f32(n, M, seed=33)
     fv, fi = api.maxk_forward(to_dev(xb), k)
