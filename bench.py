@@ -46,9 +46,10 @@ def algorithmic_bytes(N, M, k, s_in, s_val, s_idx):
     return N * M * s_in + N * k * (s_val + s_idx)
 
 
-# sources the timed kernel (fp32 rows of <= 2048 elements, one warp per row) is built from
+# sources that define the timed kernel (fp32 rows of <= 2048 elements, one warp per row)
+# and its launch configuration
 HEADLINE_SOURCES = ("rtopk_device.cuh", "rtopk_select.cuh", "rtopk_warp.cuh", "rtopk_block.cuh",
-                    "rtopk_dispatch.cuh", "rtopk_f32.cu", "launch.h", "launch_util.cu")
+                    "rtopk_dispatch.cuh", "rtopk_f32.cu", "launch_util.cu")
 
 
 def kernel_source_hash() -> str:
@@ -377,6 +378,19 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
     out["torch_topk_unsorted_us"] = t_torch_unsorted
     out["speedup_vs_torch_topk_exact"] = t_torch / out["rtopk_f32_max_iter_-1_us"]
     out["speedup_vs_torch_topk_max_iter_2"] = t_torch / out["rtopk_f32_max_iter_2_us"]
+    # bucketed approximate top-k (independent per-bucket selections): speed and
+    # hit rate against the exact result on the first 2^16 rows
+    from maxk_sparse_activations_gb300 import accuracy
+    api.rtopk_select(x, k, vals=vals, idx=idx)
+    ev = vals[: 1 << 16].cpu().numpy()
+    ei = idx[: 1 << 16].cpu().numpy()
+    for B in (2, 4, 8):
+        f = lambda: api.rtopk_select_bucketed(x, k, B, vals=vals, idx=idx)
+        f()
+        t_b = timed(f, reps) / reps * 1e3
+        acc = accuracy.compare(vals[: 1 << 16].cpu().numpy(), idx[: 1 << 16].cpu().numpy(), ev, ei)
+        out[f"bucketed_B{B}"] = {"us": t_b, "hit_rate_mean": acc["hit_rate_mean"],
+                                 "hit_rate_worst": acc["hit_rate_worst"], "r_min_mean": acc["r_min_mean"]}
     _, _, iters, st = api.rtopk_select_stats(x, k)
     it = iters.cpu().numpy()
     out["passes_exact"] = {"median": float(np.median(it)), "p90": float(np.percentile(it, 90)),

@@ -83,7 +83,7 @@ typedef enum {
   RTOPK_EINVAL_PTR = -3,   /* a required pointer is NULL (with N > 0) */
   RTOPK_EINVAL_DTYPE = -4, /* dtype is not an rtopk_dtype value */
   RTOPK_ECUDA = -5,        /* a CUDA runtime call or launch failed */
-  RTOPK_EINVAL_ARG = -6    /* eps < 0 or NaN */
+  RTOPK_EINVAL_ARG = -6    /* eps < 0 or NaN; buckets not dividing M and k */
 } rtopk_status;
 
 /*
@@ -114,6 +114,21 @@ int rtopk_select(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_it
 int rtopk_select_stats(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_iter,
                        float eps, int32_t dtype, void* vals, int32_t* idx, int32_t* iters,
                        uint32_t* status, cudaStream_t stream);
+
+/*
+ * rtopk_select_bucketed -- bucketed approximate row-wise top-k.
+ * "Approximate Top-k for Increased Parallelism" (abstract): split each vector
+ * into buckets and take many smaller top-k selections independently.
+ *
+ * Each row is split into `buckets` contiguous buckets of M / buckets columns;
+ * bucket b keeps the top-(k / buckets) of its columns under the selection of
+ * rtopk_select (max_iter / eps apply per bucket). Output as rtopk_select: k
+ * (value, index) pairs per row, indices in [0, M), ascending. buckets = 1 is
+ * rtopk_select. Requires buckets to divide both M and k (else
+ * RTOPK_EINVAL_ARG). Other arguments as for rtopk_select.
+ */
+int rtopk_select_bucketed(const void* in, int64_t N, int32_t M, int32_t k, int32_t buckets, int32_t max_iter,
+                          float eps, int32_t dtype, void* vals, int32_t* idx, cudaStream_t stream);
 
 /*
  * maxk_forward -- the MaxK nonlinearity: keep the top-k features of each row of

@@ -5,7 +5,7 @@ include/rtopk.h); ``api`` is its thin torch binding. Submodules load lazily so
 that the input generators and host-side reporting import without a GPU.
 """
 
-__all__ = ["rtopk_select", "rtopk_select_stats", "maxk_forward", "maxk_backward_scatter", "MaxK",
+__all__ = ["rtopk_select", "rtopk_select_stats", "rtopk_select_bucketed", "maxk_forward", "maxk_backward_scatter", "MaxK",
            "maxk_spgemm_forward", "maxk_sspmm_backward"]
 
 

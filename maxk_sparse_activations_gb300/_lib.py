@@ -23,7 +23,7 @@ STATUS_BAD_INDEX = 0x8
 STATUS_BAD_EDGE = 0x10
 
 #: every symbol include/rtopk.h declares
-EXPORTED = ("rtopk_select", "rtopk_select_stats", "maxk_forward", "maxk_backward_scatter",
+EXPORTED = ("rtopk_select", "rtopk_select_stats", "rtopk_select_bucketed", "maxk_forward", "maxk_backward_scatter",
             "maxk_spgemm_forward", "maxk_sspmm_backward", "rtopk_strerror", "rtopk_version")
 
 
@@ -45,6 +45,7 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         p, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
         lib.rtopk_select.argtypes = [p, i64, i32, i32, i32, f32, i32, p, p, p]
         lib.rtopk_select_stats.argtypes = [p, i64, i32, i32, i32, f32, i32, p, p, p, p, p]
+        lib.rtopk_select_bucketed.argtypes = [p, i64, i32, i32, i32, i32, f32, i32, p, p, p]
         lib.maxk_forward.argtypes = [p, i64, i32, i32, i32, f32, p, p, p]
         lib.maxk_backward_scatter.argtypes = [p, p, i64, i32, i32, p, p, p]
         lib.maxk_spgemm_forward.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p, p, p]
@@ -52,7 +53,7 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         lib.rtopk_strerror.argtypes = [ctypes.c_int]
         lib.rtopk_strerror.restype = ctypes.c_char_p
         lib.rtopk_version.argtypes = []
-        for name in ("rtopk_select", "rtopk_select_stats", "maxk_forward", "maxk_backward_scatter",
+        for name in ("rtopk_select", "rtopk_select_stats", "rtopk_select_bucketed", "maxk_forward", "maxk_backward_scatter",
                      "maxk_spgemm_forward", "maxk_sspmm_backward", "rtopk_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib

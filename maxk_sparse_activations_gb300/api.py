@@ -92,6 +92,29 @@ def rtopk_select_stats(x: torch.Tensor, k: int, max_iter: int = -1, eps: float =
     return vals, idx, iters, status
 
 
+def rtopk_select_bucketed(x: torch.Tensor, k: int, buckets: int, max_iter: int = -1, eps: float = 0.0, *,
+                          vals: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None):
+    """Bucketed approximate top-k: each row split into `buckets` column blocks,
+    each keeping its top-(k / buckets). Returns (vals N x k, idx N x k int32)."""
+    _need_cuda_2d(x, "x")
+    if x.dtype == torch.float32:
+        dtype = _lib.RTOPK_F32
+    elif x.dtype == torch.bfloat16:
+        dtype = _lib.RTOPK_BF16
+    else:
+        raise ValueError("x must be float32 or bfloat16")
+    N, M = x.shape
+    if vals is None:
+        vals = _empty_like_home((N, k), x.dtype, x)
+    if idx is None:
+        idx = _empty_like_home((N, k), torch.int32, x)
+    rc = _lib.load().rtopk_select_bucketed(x.data_ptr(), N, M, int(k), int(buckets), int(max_iter), float(eps),
+                                           dtype, vals.data_ptr(), idx.data_ptr(), _stream_ptr(stream, x.device))
+    _lib.check(rc, "rtopk_select_bucketed")
+    return vals, idx
+
+
 def maxk_forward(x: torch.Tensor, k: int, max_iter: int = -1, eps: float = 0.0, *,
                  vals: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None):

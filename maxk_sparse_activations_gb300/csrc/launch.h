@@ -23,6 +23,8 @@ struct SelectArgs {
 cudaError_t launch_select_f32(const SelectArgs& a, cudaStream_t s);
 // bf16 input; int16 indices when idx16, else int32.
 cudaError_t launch_select_bf16(const SelectArgs& a, bool idx16, cudaStream_t s);
+// Bucketed approximate top-k: B buckets per row, k / B kept per bucket (int32 indices).
+cudaError_t launch_select_bucketed(const SelectArgs& a, int dtype_bf16, int buckets, cudaStream_t s);
 // MaxK backward scatter (bf16 values, int16 indices).
 cudaError_t launch_maxk_backward(const uint16_t* dy, const int16_t* idx, int64_t N, int M, int k,
                                  uint16_t* grad, uint32_t* status, cudaStream_t s);

@@ -35,7 +35,14 @@ namespace {
 constexpr uint32_t kStatusBadIndex = 0x8u;
 constexpr uint32_t kStatusBadEdge = 0x10u;
 constexpr int kThreads = 256;
-constexpr int kU = 4;  // edges whose rows are in flight together
+#ifndef RTOPK_SPMM_U
+#define RTOPK_SPMM_U 4
+#endif
+#ifndef RTOPK_SPMM_HEAVY_WARPS
+#define RTOPK_SPMM_HEAVY_WARPS 8
+#endif
+constexpr int kU = RTOPK_SPMM_U;  // edges whose rows are in flight together
+constexpr int kHeavyThreads = 32 * RTOPK_SPMM_HEAVY_WARPS;  // warps sharing one heavy row
 // Rows with more edges than this are split over the warps of one block.
 constexpr int64_t kHeavyEdges = 512;
 
@@ -135,13 +142,13 @@ spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict
   if (status != nullptr && st != 0u) atomicOr(status, st);
 }
 
-// Destination rows with more than `heavy` edges: one block per row. Warp q
-// adds the edge chunks q, q + W, ... (chunks of `heavy` edges, each in edge
-// order) into its own accumulator; the W partial rows are then summed in warp
-// order. Deterministic, but the terms of such a row are not added in plain
+// Destination rows with more than `heavy` edges: one block (up to
+// kHeavyThreads / 32 warps) per row. Warp q adds the edge chunks q, q + W, ... (chunks of `heavy` edges,
+// each in edge order) into its own accumulator; the W partial rows are then
+// summed in warp order. Deterministic, but the terms of such a row are not added in plain
 // edge order (the bound on the difference is in the C ABI header).
 template <int KS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kHeavyThreads)
 spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
                     const float* __restrict__ w, int64_t n_dst, int64_t n_src,
                     const uint16_t* __restrict__ sp_data, const int16_t* __restrict__ sp_index, int M, int k,
@@ -152,9 +159,15 @@ spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restri
   const int wpb = blockDim.x >> 5;
   float* acc = acc_all + size_t(wib) * M;
   uint32_t st = 0;
-  for (int64_t i = blockIdx.x; i < n_dst; i += gridDim.x) {
+  // every warp reads the same 32 row lengths, so the ballot is block-uniform
+  for (int64_t i0 = int64_t(blockIdx.x) * 32; i0 < n_dst; i0 += int64_t(gridDim.x) * 32) {
+    const int64_t il = i0 + lane;
+    const bool is_heavy = il < n_dst && (row_ptr[il + 1] - row_ptr[il]) > heavy;
+    unsigned todo = __ballot_sync(0xffffffffu, is_heavy);
+    while (todo != 0u) {
+    const int64_t i = i0 + (__ffs(todo) - 1);
+    todo &= todo - 1u;
     const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
-    if (e1 - e0 <= heavy) continue;  // block-uniform
     zero_row(acc, M, lane, vec);
     __syncwarp();
     for (int64_t c0 = e0 + int64_t(wib) * heavy; c0 < e1; c0 += int64_t(wpb) * heavy) {
@@ -169,6 +182,7 @@ spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restri
       __stcs(o + m, sum);
     }
     __syncthreads();
+    }
   }
   if (status != nullptr && st != 0u) atomicOr(status, st);
 }
@@ -244,6 +258,17 @@ cudaError_t launch_rows(Kern kern, int64_t rows, size_t smem_per_warp, cudaStrea
   return blocks > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
+// Heavy rows: as many warps per block as the 48 KB of shared accumulators allow
+// (up to kHeavyThreads / 32), one block per heavy row.
+template <typename Kern>
+cudaError_t launch_heavy(Kern kern, int64_t rows, size_t smem_per_warp, int& threads, int& blocks) {
+  int wpb = int((48 * 1024) / smem_per_warp);
+  wpb = wpb > kHeavyThreads / 32 ? kHeavyThreads / 32 : (wpb < 1 ? 1 : wpb);
+  threads = wpb * 32;
+  blocks = persistent_blocks(reinterpret_cast<const void*>(kern), threads, smem_per_warp * wpb, rows);
+  return blocks > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 }  // namespace
 
 cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const float* w, int64_t n_dst,
@@ -262,7 +287,7 @@ cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const 
         row_ptr, col, w, n_dst, n_src, sp_data, sp_index, M, k, kHeavyEdges, vec, out, status);           \
     e = cudaGetLastError();                                                                               \
     if (e != cudaSuccess) return e;                                                                       \
-    e = launch_rows(spgemm_heavy_kernel<KS>, n_dst * (threads / 32), smem_warp, s, threads, blocks);      \
+    e = launch_heavy(spgemm_heavy_kernel<KS>, (n_dst + 31) / 32, smem_warp, threads, blocks);                         \
     if (e != cudaSuccess) return e;                                                                       \
     spgemm_heavy_kernel<KS><<<blocks, threads, smem_warp * (threads / 32), s>>>(                          \
         row_ptr, col, w, n_dst, n_src, sp_data, sp_index, M, k, kHeavyEdges, vec, out, status);           \

@@ -37,6 +37,18 @@ int rtopk_select(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_it
   return rtopk_select_stats(in, N, M, k, max_iter, eps, dtype, vals, idx, nullptr, nullptr, stream);
 }
 
+int rtopk_select_bucketed(const void* in, int64_t N, int32_t M, int32_t k, int32_t buckets, int32_t max_iter,
+                          float eps, int32_t dtype, void* vals, int32_t* idx, cudaStream_t stream) {
+  if (dtype != RTOPK_F32 && dtype != RTOPK_BF16) return RTOPK_EINVAL_DTYPE;
+  if (N < 0 || M < 1 || M > RTOPK_MAX_M) return RTOPK_EINVAL_SHAPE;
+  if (k < 1 || k > M) return RTOPK_EINVAL_K;
+  if (buckets < 1 || M % buckets != 0 || k % buckets != 0) return RTOPK_EINVAL_ARG;
+  const int rc = check_select(in, N, M, k, eps, vals, idx);
+  if (rc != RTOPK_OK || N == 0) return rc;
+  rtopk::SelectArgs a{in, N, M, k, max_iter, eps, vals, idx, nullptr, nullptr};
+  return from_cuda(rtopk::launch_select_bucketed(a, dtype == RTOPK_BF16, buckets, stream));
+}
+
 int maxk_forward(const void* in_bf16, int64_t N, int32_t M, int32_t k, int32_t max_iter, float eps,
                  void* vals_bf16, int16_t* idx, cudaStream_t stream) {
   const int rc = check_select(in_bf16, N, M, k, eps, vals_bf16, idx);
@@ -90,7 +102,7 @@ const char* rtopk_strerror(int code) {
     case RTOPK_EINVAL_PTR: return "a required device pointer is NULL";
     case RTOPK_EINVAL_DTYPE: return "unknown dtype: use RTOPK_F32 or RTOPK_BF16";
     case RTOPK_ECUDA: return "a CUDA runtime call or kernel launch failed";
-    case RTOPK_EINVAL_ARG: return "invalid eps: need eps >= 0";
+    case RTOPK_EINVAL_ARG: return "invalid argument: need eps >= 0, and buckets dividing both M and k";
     default: return "unknown rtopk status code";
   }
 }

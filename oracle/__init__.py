@@ -22,6 +22,10 @@ Functions (each follows the page and section named in ``rtopk_oracle.c``):
 * ``maxk_backward(dy, idx, M)`` -- the MaxK backward scatter: the gradient row
   is zero except at the kept positions. ("MaxK-GNN ...", "How MaxK-GNN works",
   "Asymmetric passes, one mask".)
+* ``bucketed_topk(x, k, buckets, max_iter, eps)`` -- bucketed approximate top-k:
+  the replay above applied to each of ``buckets`` contiguous column blocks of
+  every row with k / buckets kept per block, indices shifted to the row.
+  ("Approximate Top-k for Increased Parallelism", abstract.)
 * ``spgemm_cbsr(graph, sp_data, sp_index, M)`` -- MaxK-GNN forward aggregation:
   each destination row sums its neighbours' CBSR rows, scattered to their
   columns, in edge order (binary32, no FMA). ("MaxK-GNN ...", "How MaxK-GNN
@@ -184,3 +188,16 @@ def sspmm_cbsr(t_ptr, t_row, t_w, n_dst: int, dout, sp_index) -> np.ndarray:
                                    _ptr(do), _ptr(si), M, k, _ptr(out))
     _check(rc, "sspmm_cbsr")
     return out
+
+
+def bucketed_topk(x: np.ndarray, k: int, buckets: int, max_iter: int = -1, eps: float = 0.0):
+    """Bucketed top-k: per row, each of `buckets` column blocks keeps its
+    top-(k / buckets) by the replay; returns (values, int32 indices), N x k."""
+    N, M = x.shape
+    if M % buckets or k % buckets:
+        raise ValueError("buckets must divide M and k")
+    mb, kb = M // buckets, k // buckets
+    xb = np.ascontiguousarray(x).reshape(N * buckets, mb)
+    vals, idx, _ = replay(xb, kb, max_iter, eps)
+    offset = (np.arange(N * buckets) % buckets * mb).astype(np.int32)[:, None]
+    return vals.reshape(N, k), (idx + offset).reshape(N, k)

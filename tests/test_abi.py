@@ -62,6 +62,11 @@ def test_argument_errors_launch_nothing(lib):
     assert lib.maxk_backward_scatter(None, None, 5, 8, 2, None, None, None) == -3
     assert lib.maxk_backward_scatter(None, None, 5, 9000, 2, None, None, None) == -1
     assert lib.maxk_backward_scatter(None, None, 0, 8, 2, None, None, None) == 0
+    Bk = lib.rtopk_select_bucketed
+    assert Bk(None, 10, 256, 32, 3, -1, 0.0, 0, None, None, None) == -6   # 3 does not divide 256
+    assert Bk(None, 10, 256, 30, 4, -1, 0.0, 0, None, None, None) == -6   # 4 does not divide 30
+    assert Bk(None, 10, 256, 32, 4, -1, 0.0, 0, None, None, None) == -3   # NULL pointers
+    assert Bk(None, 0, 256, 32, 4, -1, 0.0, 0, None, None, None) == 0
     F = lib.maxk_spgemm_forward
     assert F(None, None, None, -1, 4, None, None, 8, 2, None, None, None) == -1   # n_dst < 0
     assert F(None, None, None, 4, 4, None, None, 8, 9, None, None, None) == -2    # k > M

@@ -239,3 +239,19 @@ def test_rejects_invalid_rows(oracle_mod):
         x[0, 3] = bad
         with pytest.raises(ValueError):
             oracle_mod.replay(x, 2)
+
+
+def test_bucketed_reduces_to_exact_and_argmax(oracle_mod):
+    """Bucketed top-k ("Approximate Top-k for Increased Parallelism"): one bucket
+    is the plain selection; k buckets keep each bucket's maximum, first
+    occurrence (numpy argmax)."""
+    x = synth.make("int_ties", 300, 256, seed=17)
+    v1, i1 = oracle_mod.bucketed_topk(x, 32, 1)
+    v0, i0, _ = oracle_mod.replay(x, 32)
+    np.testing.assert_array_equal(i1, i0)
+    _, ik = oracle_mod.bucketed_topk(x, 32, 32)
+    want = np.argmax(x.reshape(300, 32, 8), axis=2) + np.arange(32) * 8
+    np.testing.assert_array_equal(ik, want)
+    v4, i4 = oracle_mod.bucketed_topk(synth.normal_f32(200, 256, seed=3), 32, 4)
+    assert np.all(np.diff(i4, axis=1) > 0)
+    assert np.all((i4 // 64) == np.repeat(np.arange(4), 8)[None, :])

@@ -257,3 +257,15 @@ def test_pinned_host_buffers_zero_copy():
     torch.cuda.synchronize()
     bv, bi, _ = oracle.replay(xb, 32)
     assert_same_selection(fv.view(torch.int16).numpy().view(np.uint16), fi.numpy(), bv, bi, what="pinned bf16")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,k,B", [(256, 32, 2), (256, 32, 4), (256, 32, 8), (256, 32, 32), (1024, 128, 8),
+                                   (4096, 64, 4), (120, 12, 3)])
+def test_bucketed_topk(M, k, B, dtype):
+    x = synth.make("normal", 3000, M, seed=B, dtype=dtype)
+    for m in (-1, 2):
+        v, i = api.rtopk_select_bucketed(to_dev(x), k, B, m)
+        torch.cuda.synchronize()
+        ov, oi = oracle.bucketed_topk(x, k, B, m)
+        assert_same_selection(v, i, ov, oi, what=f"bucketed M={M} k={k} B={B} {dtype} max_iter={m}")
