@@ -338,7 +338,7 @@ def run_gb300(args, rank: int, world: int):
                          "frac": gbs / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                          else "fallback", "algorithmic_bytes_per_launch": bytes_step,
-                         "kernel": "rtopk_select_kernel<float,G=2,W=1,FULL>",
+                         "kernel": "rtopk_warp_kernel<float,G=2,EXACT,L=0,int32>",
                          "traffic_source": os.path.relpath(prof, ROOT) if prof else None},
             "cpu_baseline": cpu,
             "e2e": {"value": world * N_ROWS / (ms_e2e * 1e-3), "unit": "rows/s",

@@ -10,9 +10,15 @@
 // as the warp kernel. A pass sums the eight warp counts through shared
 // memory (double-buffered slots: one barrier per pass). With LB > 0, once
 // k < c(lo) <= 32 LB the block writes its elements >= lo, in index order, to a
-// shared list and warp 0 alone finishes the search and the CBSR row from the
-// list (finish_from_list), so the long tail of passes costs one warp and no
-// barriers. Arithmetic and branch decisions are those of the warp kernel.
+// shared list, and the rest of the search counts list entries only:
+//  * LB = 8 (list <= 256, k <= 128): warp 0 alone finishes the search and the
+//    CBSR row from the list (finish_from_list): no barriers in the tail;
+//  * LB = 64 (list <= 2048, k <= 1024): all eight warps keep going, each lane
+//    holding 8 list entries instead of its 4 G row elements, and the CBSR row
+//    is written from the list through warp ballots and per-warp prefixes.
+// For bf16 rows whose pass counts are not requested the search stops once
+// the kept set is final (bf16_single_value). Arithmetic and branch decisions
+// are those of the warp kernel.
 #pragma once
 
 #include "rtopk_warp.cuh"
@@ -20,7 +26,7 @@
 namespace rtopk {
 
 constexpr int kBlockWarps = 8;
-constexpr int kBlockList = 256;  // compaction list capacity (LB = 8 entries per lane)
+constexpr int kBlockList = 2048;  // compaction list capacity (8 warps x 8 entries per lane)
 
 struct BlockShared {
   unsigned cnt[2][kBlockWarps];
@@ -85,11 +91,79 @@ __device__ __forceinline__ void block_compact_ge(const float (&x)[G][V], float l
   __syncthreads();
 }
 
-// Two resident blocks per SM (at most 128 registers a thread): at M = 8192 a
-// thread holds 32 elements, and one block per SM leaves too few warps to hide
-// the per-pass barrier and reduction latency.
+// LB = 64: the eight warps finish the search over the shared list of the
+// n <= 2048 elements >= lo (entry e at warp e / 256, slot (e / 32) % 8,
+// lane e % 32 -- entry order is index order) and write the CBSR row.
+template <bool EXACT, bool BF16STOP, typename T, typename IdxT, typename BlockSum>
+__device__ __forceinline__ void block_finish_from_list(BlockShared& sh, BlockSum block_sum, int n, float lo,
+                                                       float hi, int& it, int k, int limit, bool cap_is_safety,
+                                                       float eps, int w, int lane, T* __restrict__ vals,
+                                                       IdxT* __restrict__ idx, int64_t obase, uint32_t& st,
+                                                       bool bf16_stop) {
+  constexpr int S = 8;
+  float lv[S][1];
+  int lj[S];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int e = w * 256 + s * 32 + lane;
+    const float2 p = (e < n) ? sh.list[e] : make_float2(neg_inf(), 0.0f);
+    lv[s][0] = p.x;
+    lj[s] = __float_as_int(p.y);
+  }
+  int c_lo = n;
+  bool dummy = false;
+  auto count_list = [&](float mid) { return block_sum(lane_count_lt<S, 1>(lv, mid)); };
+  search_passes<EXACT, 0, decltype(count_list), BF16STOP>(count_list, kBlockWarps * 32 * S, k, limit,
+                                                          cap_is_safety, eps, lo, hi, it, c_lo, dummy, st,
+                                                          bf16_stop);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  unsigned bS[S], bB[S];
+  int tS = 0, tB = 0;
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const bool sf = lv[s][0] >= hi;
+    const bool af = lv[s][0] >= lo;
+    bS[s] = __ballot_sync(0xffffffffu, sf);
+    bB[s] = __ballot_sync(0xffffffffu, af && !sf);
+    tS += __popc(bS[s]);
+    tB += __popc(bB[s]);
+  }
+  if (lane == 0) { sh.tot[w][0] = tS; sh.tot[w][1] = tB; }
+  __syncthreads();
+  int runS = 0, runB = 0, sizeS = 0;
+#pragma unroll
+  for (int i = 0; i < kBlockWarps; ++i) {
+    sizeS += sh.tot[i][0];
+    if (i < w) { runS += sh.tot[i][0]; runB += sh.tot[i][1]; }
+  }
+  const int need = max(k - sizeS, 0);
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const int rS = runS + __popc(bS[s] & lt_mask);
+    const int rB = runB + __popc(bB[s] & lt_mask);
+    const bool sf = (bS[s] >> lane) & 1u;
+    const bool bf = (bB[s] >> lane) & 1u;
+    const int pos = rS + min(rB, need);
+    if ((sf || (bf && rB < need)) && pos < k) {
+      vals[obase + pos] = out_value(lv[s][0], vals);
+      idx[obase + pos] = IdxT(lj[s]);
+    }
+    runS += __popc(bS[s]);
+    runB += __popc(bB[s]);
+  }
+}
+
+// Resident blocks per SM: at M = 8192 a thread holds 32 elements and one block
+// per SM leaves too few warps to hide the per-pass barrier and reduction
+// latency, so at least two (<= 128 registers a thread); rows of <= 16 elements
+// a thread keep three.
+template <int NE>
+struct BlockOcc {
+  static constexpr int value = NE <= 16 ? 3 : 2;
+};
+
 template <typename T, int G, bool EXACT, int LB, typename IdxT>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, BlockOcc<G * ElemTraits<T>::V>::value)
 rtopk_block_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_iter, float eps, bool full,
                    bool vec, T* __restrict__ vals, IdxT* __restrict__ idx, int* __restrict__ iters,
                    uint32_t* __restrict__ status) {
@@ -102,7 +176,8 @@ rtopk_block_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_it
   constexpr int NF = 2 * G;
   constexpr int NW = (NF + FPW - 1) / FPW;
   constexpr unsigned FMASK = (1u << FB) - 1u;
-  static_assert(LB == 0 || 32 * LB <= kBlockList, "list capacity");
+  static_assert(LB == 0 || LB == 8 || LB == 64, "list modes");
+  static_assert(32 * LB <= kBlockList, "list capacity");
 
   __shared__ BlockShared sh;
   const int lane = threadIdx.x & 31;
@@ -168,20 +243,32 @@ rtopk_block_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_it
       lo = hi;
       hi = pos_inf();
     } else {
-      eq = search_passes<EXACT, LB>([&](float mid) { return block_sum(lane_count_lt<G, V>(x, mid)); },
-                                    W * 32 * NE, k, limit, cap_is_safety, eps, lo, hi, it, c_lo, comp, st);
+      auto count_row = [&](float mid) { return block_sum(lane_count_lt<G, V>(x, mid)); };
+      eq = search_passes<EXACT, LB, decltype(count_row), (V == 8)>(count_row, W * 32 * NE, k, limit,
+                                                                   cap_is_safety, eps, lo, hi, it, c_lo, comp,
+                                                                   st, iters == nullptr);
     }
     comp = comp && ok;
     const int64_t obase = r * int64_t(k);
 
-    if (LB > 0 && comp) {
+    if (LB == 8 && comp) {
       // ---- warp 0 finishes from the compacted list of the c(lo) elements >= lo
       block_compact_ge<G, V>(x, lo, w, lane, sh);
       if (w == 0) {
-        finish_from_list<EXACT, (LB > 0 ? LB : 1), T, IdxT>(sh.list, c_lo, lo, hi, it, k, limit,
-                                                           cap_is_safety, eps, lane, vals, idx, obase, st);
+        finish_from_list<EXACT, 8, T, IdxT>(sh.list, c_lo, lo, hi, it, k, limit, cap_is_safety, eps, lane,
+                                            vals, idx, obase, st);
         if (iters != nullptr && lane == 0) iters[r] = it;
       }
+      __syncthreads();
+      continue;
+    }
+    if (LB == 64 && comp) {
+      // ---- the block finishes from the compacted list (8 entries per lane)
+      block_compact_ge<G, V>(x, lo, w, lane, sh);
+      block_finish_from_list<EXACT, (V == 8), T, IdxT>(sh, block_sum, c_lo, lo, hi, it, k, limit,
+                                                       cap_is_safety, eps, w, lane, vals, idx, obase, st,
+                                                       iters == nullptr);
+      if (iters != nullptr && w == 0 && lane == 0) iters[r] = it;
       __syncthreads();
       continue;
     }

@@ -38,16 +38,23 @@ cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s
   return cudaGetLastError();
 }
 
-// One 256-thread block per row for rows longer than kWarpMaxM elements;
-// LB = 8 hands the tail of the search to warp 0 once c(lo) <= 256.
+// One 256-thread block per row for rows longer than kWarpMaxM elements. Once
+// c(lo) fits the shared list, the search tail runs on the list: warp 0 alone
+// for lists of <= 256 (k <= 128), all warps for lists of <= 2048 (k <= 1024).
 template <typename T, int G, typename IdxT>
 cudaError_t launch_block(const SelectArgs& a, bool full, bool vec, cudaStream_t s) {
   constexpr int kThreads = 256;
   const bool exact = a.max_iter < 0 && a.eps == 0.0f;
-  const bool list = 2 * a.k <= kBlockList;
+  const int LB = (a.k <= 128) ? 8 : (a.k <= 1024 ? 64 : 0);
   using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);
-  K kern = list ? (exact ? rtopk_block_kernel<T, G, true, 8, IdxT> : rtopk_block_kernel<T, G, false, 8, IdxT>)
-                : (exact ? rtopk_block_kernel<T, G, true, 0, IdxT> : rtopk_block_kernel<T, G, false, 0, IdxT>);
+  K kern;
+  if (LB == 8) {
+    kern = exact ? rtopk_block_kernel<T, G, true, 8, IdxT> : rtopk_block_kernel<T, G, false, 8, IdxT>;
+  } else if (LB == 64) {
+    kern = exact ? rtopk_block_kernel<T, G, true, 64, IdxT> : rtopk_block_kernel<T, G, false, 64, IdxT>;
+  } else {
+    kern = exact ? rtopk_block_kernel<T, G, true, 0, IdxT> : rtopk_block_kernel<T, G, false, 0, IdxT>;
+  }
   const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), kThreads, 0, a.N);
   if (blocks <= 0) return cudaErrorInvalidConfiguration;
   kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, a.max_iter, a.eps, full, vec,

@@ -120,16 +120,40 @@ __device__ __forceinline__ unsigned lane_count_lt(const float (&x)[G][V], float 
   return lt0 + lt1;
 }
 
+// True when [lo, hi) holds at most one bf16 value (lo <= hi finite). For bf16
+// data every count c(t) only changes at bf16 values, so from then on further
+// passes move lo and hi without changing S = {x >= hi} or B = {lo <= x < hi}:
+// the kept set is final. (It cannot hold none: c(lo) >= k > c(hi).)
+__device__ __forceinline__ bool bf16_single_value(float lo, float hi) {
+  // l = smallest bf16 >= lo (round toward +inf)
+  const uint32_t bl = __float_as_uint(lo);
+  uint32_t l = bl;
+  if (bl & 0xffffu) l = (bl & 0x80000000u) ? (bl & 0xffff0000u) : ((bl & 0xffff0000u) + 0x10000u);
+  // u = largest bf16 < hi
+  const uint32_t bh = __float_as_uint(hi);
+  uint32_t u;
+  if (bh & 0xffffu) {
+    u = (bh & 0x80000000u) ? ((bh & 0xffff0000u) + 0x10000u) : (bh & 0xffff0000u);
+  } else if ((bh & 0x7fffffffu) == 0u) {
+    u = 0x80010000u;  // hi = +-0: the largest bf16 below it is -(smallest subnormal)
+  } else {
+    u = (bh & 0x80000000u) ? (bh + 0x10000u) : (bh - 0x10000u);
+  }
+  return __uint_as_float(u) <= __uint_as_float(l);
+}
+
 // Bisection passes from the current (lo, hi); `count_lt_team(mid)` returns the
 // number of the team's elements below mid (identical in every thread), so a
 // pass count is total - count_lt_team(mid). Returns true when a pass found
 // c(mid) == k. With L > 0 it also stops (returning false, comp = true) right
-// after a pass that moved lo to a value with k < c(lo) <= 32 L.
-template <bool EXACT, int L, typename CountLtTeam>
+// after a pass that moved lo to a value with k < c(lo) <= 32 L. With
+// BF16STOP and `bf16_stop` set (bf16 data, pass counts not reported) it stops
+// once the kept set is final (bf16_single_value): same result, fewer passes.
+template <bool EXACT, int L, typename CountLtTeam, bool BF16STOP = false>
 __device__ __forceinline__ bool search_passes(CountLtTeam count_lt_team, int total, int k, int limit,
                                               bool cap_is_safety,
                                               float eps, float& lo, float& hi, int& it, int& c_lo, bool& comp,
-                                              uint32_t& st) {
+                                              uint32_t& st, bool bf16_stop = false) {
   for (;;) {
     if (EXACT) {
       if (it >= kSafetyCap) { st |= kStatusSafetyCap; return false; }
@@ -150,6 +174,11 @@ __device__ __forceinline__ bool search_passes(CountLtTeam count_lt_team, int tot
     c_lo = ge ? cnt : c_lo;
     if (cnt == k) return true;
     if (L > 0 && ge && cnt <= 32 * L) { comp = true; return false; }
+    // cheap necessary condition first: one bf16 value in [lo, hi) needs
+    // hi - lo < 2 bf16 ulps <= max(|lo|, |hi|) * 2^-6 (+ the subnormal spacing)
+    if (BF16STOP && bf16_stop &&
+        __fsub_rn(hi, lo) <= fmaxf(fabsf(lo), fabsf(hi)) * 0.015625f + 1e-38f && bf16_single_value(lo, hi))
+      return false;
   }
 }
 
@@ -292,8 +321,9 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
     lo = hi;           // keep the k lowest-index maxima through the fill rule:
     hi = pos_inf();    // S is empty and every maximum is borderline
   } else {
-    eq = search_passes<EXACT, L>([&](float mid) { return __reduce_add_sync(0xffffffffu, lane_count_lt<G, V>(x, mid)); }, 32 * NE, k, limit,
-                                 cap_is_safety, eps, lo, hi, it, c_lo, comp, st);
+    auto count_row = [&](float mid) { return __reduce_add_sync(0xffffffffu, lane_count_lt<G, V>(x, mid)); };
+    eq = search_passes<EXACT, L, decltype(count_row), (V == 8)>(count_row, 32 * NE, k, limit, cap_is_safety,
+                                                                 eps, lo, hi, it, c_lo, comp, st, iters == nullptr);
   }
   comp = comp && ok;
 

@@ -269,3 +269,22 @@ def test_bucketed_topk(M, k, B, dtype):
         torch.cuda.synchronize()
         ov, oi = oracle.bucketed_topk(x, k, B, m)
         assert_same_selection(v, i, ov, oi, what=f"bucketed M={M} k={k} B={B} {dtype} max_iter={m}")
+
+
+@pytest.mark.parametrize("value_set", ["normal", "int_ties", "subnormal", "uniform"])
+@pytest.mark.parametrize("M", [256, 512, 1000])
+def test_bf16_search_stops_once_kept_set_is_final(value_set, M):
+    """bf16 rows without pass counts requested stop as soon as [lo, hi) holds a
+    single bf16 value; the kept set must equal the full replay's in every mode."""
+    x = synth.make(value_set, 3000, M, seed=M, dtype="bf16")
+    xt = to_dev(x)
+    for k in (1, 32, M // 4):
+        for m, eps in ((-1, 0.0), (3, 0.0), (12, 0.0), (-1, 1e-3)):
+            v, i = api.rtopk_select(xt, k, m, eps)
+            torch.cuda.synchronize()
+            ov, oi, _ = oracle.replay(x, k, m, eps)
+            assert_same_selection(v, i, ov, oi, what=f"bf16 stop {value_set} M={M} k={k} max_iter={m} eps={eps}")
+        fv, fi = api.maxk_forward(xt, k)
+        torch.cuda.synchronize()
+        ov, oi, _ = oracle.replay(x, k)
+        assert_same_selection(fv, fi, ov, oi, what=f"maxk_forward stop {value_set} M={M} k={k}")
