@@ -391,11 +391,22 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
         acc = accuracy.compare(vals[: 1 << 16].cpu().numpy(), idx[: 1 << 16].cpu().numpy(), ev, ei)
         out[f"bucketed_B{B}"] = {"us": t_b, "hit_rate_mean": acc["hit_rate_mean"],
                                  "hit_rate_worst": acc["hit_rate_worst"], "r_min_mean": acc["r_min_mean"]}
+    # early-stop accuracy against exact on the MaxK-shaped 2^18-row block (the
+    # pages report hit rate and max / min relative error for early stopping)
+    nacc = 1 << 18
+    api.rtopk_select(x, k, vals=vals, idx=idx)
+    ev = vals[:nacc].cpu().numpy()
+    ei = idx[:nacc].cpu().numpy()
+    es = {}
+    for m in (2, 3, 4, 5, 8):
+        api.rtopk_select(x, k, m, 0.0, vals=vals, idx=idx)
+        es[f"max_iter_{m}"] = accuracy.compare(vals[:nacc].cpu().numpy(), idx[:nacc].cpu().numpy(), ev, ei)
+    out["early_stop_accuracy_vs_exact"] = es
     _, _, iters, st = api.rtopk_select_stats(x, k)
     it = iters.cpu().numpy()
     out["passes_exact"] = {"median": float(np.median(it)), "p90": float(np.percentile(it, 90)),
                            "max": int(it.max()), "frac_le_16": float(np.mean(it <= 16)),
-                           "status": int(st.item())}
+                           "histogram": np.bincount(it, minlength=1).tolist(), "status": int(st.item())}
     xb = torch.from_numpy(synth.normal_bf16(N, M, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
     fv = torch.empty((N, k), dtype=torch.bfloat16, device=dev)
     fi = torch.empty((N, k), dtype=torch.int16, device=dev)
