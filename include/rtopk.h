@@ -68,7 +68,8 @@ extern "C" {
 #define RTOPK_STATUS_BAD_INDEX  0x8u /* an sp_index entry outside [0, M) was skipped */
 #define RTOPK_STATUS_BAD_EDGE   0x10u /* aggregation: an edge endpoint outside its row range was skipped */
 
-#define RTOPK_MAX_M 8192 /* [RTopK] "Limitations": rows longer than 8192 are unsupported */
+#define RTOPK_MAX_M 8192 /* [RTopK] "Limitations": the method's row limit; all entry points but rtopk_select */
+#define RTOPK_SELECT_MAX_M 65536 /* rtopk_select / _stats: longer rows run one CTA cluster per row */
 #define RTOPK_GNN_MAX_K 256 /* largest k of the aggregation entry points */
 
 typedef enum {
@@ -78,7 +79,7 @@ typedef enum {
 
 typedef enum {
   RTOPK_OK = 0,
-  RTOPK_EINVAL_SHAPE = -1, /* N < 0, M < 1 or M > RTOPK_MAX_M */
+  RTOPK_EINVAL_SHAPE = -1, /* N < 0, M < 1 or M above the entry point's limit */
   RTOPK_EINVAL_K = -2,     /* k < 1 or k > M */
   RTOPK_EINVAL_PTR = -3,   /* a required pointer is NULL (with N > 0) */
   RTOPK_EINVAL_DTYPE = -4, /* dtype is not an rtopk_dtype value */
@@ -91,7 +92,11 @@ typedef enum {
  * [RTopK] "Problem", "Approach"; [MaxK] "The idea" (CBSR = two dense N x k arrays).
  *
  *  in        device, N x M, dtype elements (fp32 or bf16 bit patterns), read only
- *  N, M, k   rows, row length (1..8192), kept per row (1..M)
+ *  N, M, k   rows, row length (1..65536), kept per row (1..M). Rows up to 8192
+ *            elements are the pages' range; longer rows (beyond the limit the
+ *            pages state in "Limitations") run the same search with one
+ *            cluster of 2, 4 or 8 CTAs per row, exchanging pass counts through
+ *            distributed shared memory -- same results as the scalar definition
  *  max_iter  cap on counted bisection passes; < 0 = no cap (early stop off)
  *  eps       absolute precision: the search stops once (hi - lo) <= eps; >= 0
  *  dtype     RTOPK_F32 or RTOPK_BF16
@@ -210,6 +215,27 @@ int maxk_spgemm_forward(const int64_t* row_ptr, const int32_t* col_idx, const fl
 int maxk_sspmm_backward(const int64_t* t_row_ptr, const int32_t* t_dst, const float* t_edge_w, int64_t n_src,
                         int64_t n_dst, const float* dout, const int16_t* sp_index, int32_t M, int32_t k,
                         float* d_sp_data, uint32_t* status, cudaStream_t stream);
+
+/*
+ * maxk_sspmm_backward_scatter -- maxk_sspmm_backward with the MaxK backward
+ * scatter fused in: the gradient of the MaxK input, written dense.
+ * [MaxK] "Asymmetric passes, one mask" (the backward SSpMM and the MaxK
+ * backward share the forward sp_index; only kept features carry gradient).
+ *
+ *  grad[j, sp_index[j, t]] = bf16(d_sp_data[j, t]) with d_sp_data[j, t]
+ *              exactly as maxk_sspmm_backward defines it, rounded to the
+ *              nearest bf16 (ties to even); +0.0 at every other column. This
+ *              equals maxk_sspmm_backward, a round-to-nearest conversion to
+ *              bf16 and maxk_backward_scatter run in sequence, without the
+ *              n_src x k intermediate in HBM.
+ *
+ *  grad_bf16   device, n_src x M bf16, written in full
+ *  other arguments as for maxk_sspmm_backward
+ * Indices repeated within a row leave which of their values lands unspecified.
+ */
+int maxk_sspmm_backward_scatter(const int64_t* t_row_ptr, const int32_t* t_dst, const float* t_edge_w,
+                                int64_t n_src, int64_t n_dst, const float* dout, const int16_t* sp_index,
+                                int32_t M, int32_t k, void* grad_bf16, uint32_t* status, cudaStream_t stream);
 
 /* Human-readable text for an rtopk_status code (static storage, never NULL). */
 const char* rtopk_strerror(int code);

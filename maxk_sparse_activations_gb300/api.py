@@ -226,3 +226,35 @@ def maxk_sspmm_backward(t_row_ptr: torch.Tensor, t_dst: torch.Tensor, t_edge_w: 
                                          _ptr(status), _stream_ptr(stream, dout.device))
     _lib.check(rc, "maxk_sspmm_backward")
     return d_sp
+
+
+def maxk_sspmm_backward_scatter(t_row_ptr: torch.Tensor, t_dst: torch.Tensor, t_edge_w: Optional[torch.Tensor],
+                                dout: torch.Tensor, sp_index: torch.Tensor, M: Optional[int] = None, *,
+                                grad: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """maxk_sspmm_backward with the MaxK backward scatter fused in: the dense
+    bf16 gradient of the MaxK input (n_src x M), the CBSR-value gradient
+    rounded to bf16 at the forward sp_index and +0 elsewhere. M defaults to
+    the width of dout."""
+    _need_1d(t_row_ptr, "t_row_ptr", torch.int64)
+    _need_1d(t_dst, "t_dst", torch.int32)
+    if t_edge_w is not None:
+        _need_1d(t_edge_w, "t_edge_w", torch.float32)
+    _need_cuda_2d(dout, "dout")
+    _need_cuda_2d(sp_index, "sp_index")
+    if dout.dtype != torch.float32 or sp_index.dtype != torch.int16:
+        raise ValueError("dout must be float32 and sp_index int16")
+    n_dst, Md = dout.shape
+    M = Md if M is None else int(M)
+    if M != Md:
+        raise ValueError("M must equal the width of dout")
+    n_src, k = sp_index.shape
+    if t_row_ptr.numel() != n_src + 1:
+        raise ValueError("t_row_ptr must have n_src + 1 entries")
+    if grad is None:
+        grad = _empty_like_home((n_src, M), torch.bfloat16, dout)
+    rc = _lib.load().maxk_sspmm_backward_scatter(t_row_ptr.data_ptr(), t_dst.data_ptr(), _ptr(t_edge_w), n_src,
+                                                 n_dst, dout.data_ptr(), sp_index.data_ptr(), int(M), int(k),
+                                                 grad.data_ptr(), _ptr(status), _stream_ptr(stream, dout.device))
+    _lib.check(rc, "maxk_sspmm_backward_scatter")
+    return grad

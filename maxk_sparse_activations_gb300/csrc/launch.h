@@ -33,13 +33,19 @@ cudaError_t launch_maxk_backward(const uint16_t* dy, const int16_t* idx, int64_t
 cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const float* w, int64_t n_dst,
                               int64_t n_src, const uint16_t* sp_data, const int16_t* sp_index, int M, int k,
                               float* out, uint32_t* status, cudaStream_t s);
+// grad != nullptr: the MaxK scatter is fused in and grad (n_src x M bf16) is
+// written instead of d_sp.
 cudaError_t launch_sspmm_bwd(const int64_t* t_ptr, const int32_t* t_row, const float* t_w, int64_t n_src,
                              int64_t n_dst, const float* dout, const int16_t* sp_index, int M, int k,
-                             float* d_sp, uint32_t* status, cudaStream_t s);
+                             float* d_sp, uint16_t* grad, uint32_t* status, cudaStream_t s);
 
 // Persistent-grid size for `kernel` launched with `threads` threads per block:
 // SM count x resident blocks per SM (cached per device and kernel), capped at
 // the number of blocks the work needs.
 int persistent_blocks(const void* kernel, int threads, size_t smem, int64_t blocks_needed);
+// The same for a kernel launched in clusters of `cluster` CTAs: the number of
+// clusters that can be resident at once, capped at the clusters the work needs
+// (0 if none fits).
+int persistent_clusters(const void* kernel, int threads, int cluster, int64_t clusters_needed);
 
 }  // namespace rtopk

@@ -27,6 +27,8 @@
 // row, lane t owns entry t, and the gathers of U edges are issued together.
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 #include "launch.h"
 
 namespace rtopk {
@@ -187,12 +189,24 @@ spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restri
   if (status != nullptr && st != 0u) atomicOr(status, st);
 }
 
-template <int KS>
+__device__ __forceinline__ void st_stream_u4(uint16_t* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// SCATTER = false: writes d_sp (n_src x k fp32). SCATTER = true: the MaxK
+// backward scatter fused in -- writes the dense gradient row of the MaxK input
+// instead, bf16(d_sp[j, t]) (round to nearest even) at column sp_index[j, t]
+// and +0 elsewhere: each warp zeroes its shared slice of `row_stride` bf16,
+// scatters its k values, and streams the row out (16-byte stores when `vec`).
+template <int KS, bool SCATTER>
 __global__ void __launch_bounds__(kThreads)
 sspmm_bwd_kernel(const int64_t* __restrict__ t_ptr, const int32_t* __restrict__ t_row,
                  const float* __restrict__ t_w, int64_t n_src, int64_t n_dst, const float* __restrict__ dout,
                  const int16_t* __restrict__ sp_index, int M, int k, float* __restrict__ d_sp,
-                 uint32_t* __restrict__ status) {
+                 int row_stride, bool vec, uint16_t* __restrict__ grad, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(16) uint16_t grad_rows[];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
@@ -235,10 +249,30 @@ sspmm_bwd_kernel(const int64_t* __restrict__ t_ptr, const int32_t* __restrict__ 
             if (oki[q]) acc[s] = __fadd_rn(acc[s], __fmul_rn(we[q], g[q][s]));
       }
     }
+    if (!SCATTER) {
 #pragma unroll
-    for (int s = 0; s < KS; ++s) {
-      const int t = s * 32 + lane;
-      if (t < k) d_sp[j * k + t] = acc[s];
+      for (int s = 0; s < KS; ++s) {
+        const int t = s * 32 + lane;
+        if (t < k) d_sp[j * k + t] = acc[s];
+      }
+    } else {
+      uint16_t* srow = grad_rows + size_t(wib) * row_stride;
+      uint4* s4 = reinterpret_cast<uint4*>(srow);
+      for (int i = lane; i < row_stride / 8; i += 32) s4[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        const int t = s * 32 + lane;
+        if (t < k && c[s] >= 0) srow[c[s]] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[s]));
+      }
+      __syncwarp();
+      uint16_t* o = grad + j * int64_t(M);
+      if (vec) {
+        for (int i = lane; i < M / 8; i += 32) st_stream_u4(o + 8 * i, s4[i]);
+      } else {
+        for (int i = lane; i < M; i += 32) o[i] = srow[i];
+      }
+      __syncwarp();
     }
   }
   if (status != nullptr && st != 0u) atomicOr(status, st);
@@ -302,21 +336,31 @@ cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const 
 
 cudaError_t launch_sspmm_bwd(const int64_t* t_ptr, const int32_t* t_row, const float* t_w, int64_t n_src,
                              int64_t n_dst, const float* dout, const int16_t* sp_index, int M, int k,
-                             float* d_sp, uint32_t* status, cudaStream_t s) {
+                             float* d_sp, uint16_t* grad, uint32_t* status, cudaStream_t s) {
   const int ks = (k + 31) / 32;
   int threads = 0, blocks = 0;
-#define RTOPK_BWD(KS)                                                                                     \
+  // the fused scatter builds each row in a shared slice of M rounded up to 8 bf16
+  const int row_stride = (M + 7) / 8 * 8;
+  const size_t smem_warp = grad != nullptr ? size_t(row_stride) * 2 : 0;
+  const bool vec = (M % 8 == 0) && ((reinterpret_cast<uintptr_t>(grad) & 15u) == 0);
+#define RTOPK_BWD(KS, SC)                                                                                 \
   {                                                                                                       \
-    cudaError_t e = launch_rows(sspmm_bwd_kernel<KS>, n_src, 0, s, threads, blocks);                      \
+    cudaError_t e = launch_rows(sspmm_bwd_kernel<KS, SC>, n_src, smem_warp, s, threads, blocks);          \
     if (e != cudaSuccess) return e;                                                                       \
-    sspmm_bwd_kernel<KS><<<blocks, threads, 0, s>>>(t_ptr, t_row, t_w, n_src, n_dst, dout, sp_index, M, k, \
-                                                     d_sp, status);                                       \
+    sspmm_bwd_kernel<KS, SC><<<blocks, threads, smem_warp * (threads / 32), s>>>(                         \
+        t_ptr, t_row, t_w, n_src, n_dst, dout, sp_index, M, k, d_sp, row_stride, vec, grad, status);      \
     return cudaGetLastError();                                                                            \
   }
-  if (ks <= 1) RTOPK_BWD(1)
-  if (ks <= 2) RTOPK_BWD(2)
-  if (ks <= 4) RTOPK_BWD(4)
-  RTOPK_BWD(8)
+  if (grad != nullptr) {
+    if (ks <= 1) RTOPK_BWD(1, true)
+    if (ks <= 2) RTOPK_BWD(2, true)
+    if (ks <= 4) RTOPK_BWD(4, true)
+    RTOPK_BWD(8, true)
+  }
+  if (ks <= 1) RTOPK_BWD(1, false)
+  if (ks <= 2) RTOPK_BWD(2, false)
+  if (ks <= 4) RTOPK_BWD(4, false)
+  RTOPK_BWD(8, false)
 #undef RTOPK_BWD
 }
 

@@ -32,6 +32,7 @@ struct BlockShared {
   unsigned cnt[2][kBlockWarps];
   int omax[kBlockWarps];
   int omin[kBlockWarps];
+  int ofl[kBlockWarps];
   int tot[kBlockWarps][2];
   float2 list[kBlockList];
 };
@@ -217,12 +218,20 @@ rtopk_block_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_it
         mx = max_nan(mx, x[g][e]);
         mn = min_nan(mn, (full || (w * G + g) * GS + lane * V + e < M) ? x[g][e] : pos_inf());
       }
+    // an exact search whose pass count is not reported may start from the
+    // group-maximum lower end (the exact top-k set does not depend on it)
+    const bool floor_lo = EXACT && iters == nullptr && k <= W * 32;
     int omx = __reduce_max_sync(0xffffffffu, f2o(mx));
     int omn = __reduce_min_sync(0xffffffffu, f2o(mn));
-    if (lane == 0) { sh.omax[w] = omx; sh.omin[w] = omn; }
+    int ofl = floor_lo ? group_max_floor<W * 32>(mx, k) : omn;
+    if (lane == 0) { sh.omax[w] = omx; sh.omin[w] = omn; sh.ofl[w] = ofl; }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < W; ++i) { omx = max(omx, sh.omax[i]); omn = min(omn, sh.omin[i]); }
+    for (int i = 0; i < W; ++i) {
+      omx = max(omx, sh.omax[i]);
+      omn = min(omn, sh.omin[i]);
+      ofl = min(ofl, sh.ofl[i]);
+    }
     float lo = o2f(omn), hi = o2f(omx);
     const bool ok = (lo >= -1e38f && hi <= 1e38f);
     if (!ok) st |= (isfinite(lo) && isfinite(hi)) ? kStatusRange : kStatusNonFinite;
@@ -243,6 +252,7 @@ rtopk_block_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_it
       lo = hi;
       hi = pos_inf();
     } else {
+      if (floor_lo && ok) lo = fmaxf(lo, o2f(ofl));
       auto count_row = [&](float mid) { return block_sum(lane_count_lt<G, V>(x, mid)); };
       eq = search_passes<EXACT, LB, decltype(count_row), (V == 8)>(count_row, W * 32 * NE, k, limit,
                                                                    cap_is_safety, eps, lo, hi, it, c_lo, comp,

@@ -7,8 +7,8 @@
 namespace {
 
 int check_select(const void* in, int64_t N, int32_t M, int32_t k, float eps, const void* vals,
-                 const void* idx) {
-  if (N < 0 || M < 1 || M > RTOPK_MAX_M) return RTOPK_EINVAL_SHAPE;
+                 const void* idx, int32_t max_m = RTOPK_MAX_M) {
+  if (N < 0 || M < 1 || M > max_m) return RTOPK_EINVAL_SHAPE;
   if (k < 1 || k > M) return RTOPK_EINVAL_K;
   if (!(eps >= 0.0f)) return RTOPK_EINVAL_ARG;
   if (N > 0 && (in == nullptr || vals == nullptr || idx == nullptr)) return RTOPK_EINVAL_PTR;
@@ -25,7 +25,7 @@ int rtopk_select_stats(const void* in, int64_t N, int32_t M, int32_t k, int32_t 
                        int32_t dtype, void* vals, int32_t* idx, int32_t* iters, uint32_t* status,
                        cudaStream_t stream) {
   if (dtype != RTOPK_F32 && dtype != RTOPK_BF16) return RTOPK_EINVAL_DTYPE;
-  const int rc = check_select(in, N, M, k, eps, vals, idx);
+  const int rc = check_select(in, N, M, k, eps, vals, idx, RTOPK_SELECT_MAX_M);
   if (rc != RTOPK_OK || N == 0) return rc;
   rtopk::SelectArgs a{in, N, M, k, max_iter, eps, vals, idx, iters, status};
   if (dtype == RTOPK_F32) return from_cuda(rtopk::launch_select_f32(a, stream));
@@ -91,13 +91,27 @@ int maxk_sspmm_backward(const int64_t* t_row_ptr, const int32_t* t_dst, const fl
     return RTOPK_EINVAL_PTR;
   if (n_src == 0) return RTOPK_OK;
   return from_cuda(rtopk::launch_sspmm_bwd(t_row_ptr, t_dst, t_edge_w, n_src, n_dst, dout, sp_index, M, k,
-                                           d_sp_data, status, stream));
+                                           d_sp_data, nullptr, status, stream));
+}
+
+int maxk_sspmm_backward_scatter(const int64_t* t_row_ptr, const int32_t* t_dst, const float* t_edge_w,
+                                int64_t n_src, int64_t n_dst, const float* dout, const int16_t* sp_index,
+                                int32_t M, int32_t k, void* grad_bf16, uint32_t* status, cudaStream_t stream) {
+  if (n_dst < 0 || n_src < 0 || M < 1 || M > RTOPK_MAX_M) return RTOPK_EINVAL_SHAPE;
+  if (k < 1 || k > M || k > RTOPK_GNN_MAX_K) return RTOPK_EINVAL_K;
+  if (n_src > 0 && (t_row_ptr == nullptr || sp_index == nullptr || grad_bf16 == nullptr ||
+                    (n_dst > 0 && (t_dst == nullptr || dout == nullptr))))
+    return RTOPK_EINVAL_PTR;
+  if (n_src == 0) return RTOPK_OK;
+  return from_cuda(rtopk::launch_sspmm_bwd(t_row_ptr, t_dst, t_edge_w, n_src, n_dst, dout, sp_index, M, k,
+                                           nullptr, static_cast<uint16_t*>(grad_bf16), status, stream));
 }
 
 const char* rtopk_strerror(int code) {
   switch (code) {
     case RTOPK_OK: return "ok";
-    case RTOPK_EINVAL_SHAPE: return "invalid shape: need N >= 0 and 1 <= M <= 8192";
+    case RTOPK_EINVAL_SHAPE:
+      return "invalid shape: need N >= 0 and 1 <= M <= 65536 (rtopk_select) or 8192 (other entry points)";
     case RTOPK_EINVAL_K: return "invalid k: need 1 <= k <= M";
     case RTOPK_EINVAL_PTR: return "a required device pointer is NULL";
     case RTOPK_EINVAL_DTYPE: return "unknown dtype: use RTOPK_F32 or RTOPK_BF16";

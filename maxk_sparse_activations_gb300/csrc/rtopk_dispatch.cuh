@@ -4,6 +4,7 @@
 #include "launch.h"
 #include "rtopk_select.cuh"
 #include "rtopk_block.cuh"
+#include "rtopk_cluster.cuh"
 
 namespace rtopk {
 
@@ -114,6 +115,45 @@ cudaError_t launch_long_rows(const SelectArgs& a, cudaStream_t s) {
       if constexpr (GS * 4 < 8192) return launch_block<T, 8, IdxT>(a, full, vec, s);
       return cudaErrorInvalidValue;
   }
+}
+
+// Rows of 8193..65536 elements: one cluster of C CTAs per row, 32 elements
+// per lane (8192 per CTA), C the smallest of 2, 4, 8 that covers the row --
+// the fewer CTAs a row takes, the more rows are in flight at once.
+template <typename T, int C, typename IdxT>
+cudaError_t launch_cluster_c(const SelectArgs& a, cudaStream_t s) {
+  constexpr int V = ElemTraits<T>::V;
+  constexpr int G = 32 / V;
+  constexpr int kRow = C * kBlockWarps * G * 32 * V;
+  const bool vec = (a.M % V == 0) && aligned16(a.in);
+  const bool full = vec && a.M == kRow;
+  const bool exact = a.max_iter < 0 && a.eps == 0.0f;
+  using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);
+  K kern = exact ? rtopk_cluster_kernel<T, G, true, C, IdxT> : rtopk_cluster_kernel<T, G, false, C, IdxT>;
+  const int clusters = persistent_clusters(reinterpret_cast<const void*>(kern), 256, C, a.N);
+  if (clusters <= 0) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(unsigned(clusters * C));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(a.in), a.N, a.M, a.k, a.max_iter, a.eps, full, vec,
+                            static_cast<T*>(a.vals), static_cast<IdxT*>(a.idx), a.iters, a.status);
+}
+
+template <typename T, typename IdxT>
+cudaError_t launch_cluster_rows(const SelectArgs& a, cudaStream_t s) {
+  if (a.M <= 2 * 8192) return launch_cluster_c<T, 2, IdxT>(a, s);
+  if (a.M <= 4 * 8192) return launch_cluster_c<T, 4, IdxT>(a, s);
+  if (a.M <= 8 * 8192) return launch_cluster_c<T, 8, IdxT>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace rtopk

@@ -120,6 +120,23 @@ __device__ __forceinline__ unsigned lane_count_lt(const float (&x)[G][V], float 
   return lt0 + lt1;
 }
 
+// A lower end for an exact search. The TEAM_LANES lanes that share a row are
+// split into the largest number of equal lane groups that is still >= k
+// (groups never span warps); each group holds an element >= its group
+// maximum, so at least k elements of the row are >= the smallest group
+// maximum: c(that value) >= k, a valid lower end whenever k <= TEAM_LANES.
+// `mx` is the lane's maximum (-inf for a lane of pads, which leaves the bound
+// at -inf). Returns this warp's smallest group maximum as an ordered integer.
+template <int TEAM_LANES>
+__device__ __forceinline__ int group_max_floor(float mx, int k) {
+  int groups = TEAM_LANES;
+  for (int d = 1; d < 32 && (groups >> 1) >= k; d <<= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    groups >>= 1;
+  }
+  return __reduce_min_sync(0xffffffffu, f2o(mx));
+}
+
 // True when [lo, hi) holds at most one bf16 value (lo <= hi finite). For bf16
 // data every count c(t) only changes at bf16 values, so from then on further
 // passes move lo and hi without changing S = {x >= hi} or B = {lo <= x < hi}:

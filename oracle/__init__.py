@@ -33,6 +33,12 @@ Functions (each follows the page and section named in ``rtopk_oracle.c``):
 * ``sspmm_cbsr(tgraph, dout, sp_index, n_dst)`` -- the backward sampled product:
   the gradient of each CBSR value sums, over the source row's out-edges in
   order, the edge weight times dout at (destination, sp_index).
+* ``round_bf16(x)`` -- binary32 to the nearest bf16, ties to an even last bit,
+  chosen by comparing the exact distances to the two neighbouring bf16 values.
+* ``sspmm_scatter(tgraph, dout, sp_index, n_dst, M)`` -- the backward sampled
+  product followed by the MaxK backward scatter of its bf16-rounded values:
+  the dense gradient of the MaxK input. ("MaxK-GNN ...", "Asymmetric passes,
+  one mask".)
 
 bf16 inputs are widened exactly to binary32 (the 16 bits become the top half of
 the word) and run through the same functions; kept values are the original
@@ -201,3 +207,28 @@ def bucketed_topk(x: np.ndarray, k: int, buckets: int, max_iter: int = -1, eps: 
     vals, idx, _ = replay(xb, kb, max_iter, eps)
     offset = (np.arange(N * buckets) % buckets * mb).astype(np.int32)[:, None]
     return vals.reshape(N, k), (idx + offset).reshape(N, k)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Finite binary32 -> nearest bf16 bit pattern, ties to an even last bit.
+
+    The two candidates are the bf16 values that bracket x: its top 16 bits
+    (toward zero) and the next bf16 away from zero. Their distances to x are
+    exact in float64, so the nearer one is picked exactly.
+    """
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lo = (b >> np.uint32(16)).astype(np.uint32)          # toward zero
+    hi = lo + np.uint32(1)                                # one bf16 step away from zero
+    xv = b.view(np.float32).astype(np.float64)
+    lv = (lo << np.uint32(16)).view(np.float32).astype(np.float64)
+    hv = (hi << np.uint32(16)).view(np.float32).astype(np.float64)
+    dl, dh = np.abs(xv - lv), np.abs(hv - xv)
+    pick_hi = (dh < dl) | ((dh == dl) & ((lo & np.uint32(1)) == 1))
+    return np.where(pick_hi, hi, lo).astype(np.uint16)
+
+
+def sspmm_scatter(t_ptr, t_row, t_w, n_dst: int, dout, sp_index, M: int) -> np.ndarray:
+    """Backward sampled product, rounded to bf16 and scattered to a dense
+    n_src x M bf16 (bit pattern) gradient of the MaxK input."""
+    d_sp = sspmm_cbsr(t_ptr, t_row, t_w, n_dst, dout, sp_index)
+    return maxk_backward(round_bf16(d_sp), sp_index, M)

@@ -48,7 +48,11 @@ def test_argument_errors_launch_nothing(lib):
     # every call below must return before any CUDA call (no GPU here)
     S = lambda *a: lib.rtopk_select(*a)
     assert S(None, 10, 0, 1, -1, 0.0, 0, None, None, None) == -1          # M < 1
-    assert S(None, 10, 8193, 1, -1, 0.0, 0, None, None, None) == -1       # M > 8192
+    assert S(None, 10, 65537, 1, -1, 0.0, 0, None, None, None) == -1      # M > 65536
+    assert S(None, 10, 8193, 1, -1, 0.0, 0, None, None, None) == -3       # long rows accepted: NULL pointers
+    assert lib.maxk_forward(None, 10, 8193, 1, -1, 0.0, None, None, None) == -1  # maxk_forward: M <= 8192
+    Bk = lib.rtopk_select_bucketed
+    assert Bk(None, 10, 16384, 32, 2, -1, 0.0, 0, None, None, None) == -1  # bucketed: M <= 8192
     assert S(None, -1, 8, 1, -1, 0.0, 0, None, None, None) == -1          # N < 0
     assert S(None, 10, 8, 0, -1, 0.0, 0, None, None, None) == -2          # k < 1
     assert S(None, 10, 8, 9, -1, 0.0, 0, None, None, None) == -2          # k > M
@@ -77,3 +81,8 @@ def test_argument_errors_launch_nothing(lib):
     assert B(None, None, None, 4, 4, None, None, 9000, 2, None, None, None) == -1  # M > 8192
     assert B(None, None, None, 4, 4, None, None, 8, 2, None, None, None) == -3
     assert B(None, None, None, 0, 4, None, None, 8, 2, None, None, None) == 0
+    BS = lib.maxk_sspmm_backward_scatter
+    assert BS(None, None, None, 4, 4, None, None, 9000, 2, None, None, None) == -1  # M > 8192
+    assert BS(None, None, None, 4, 4, None, None, 8, 9, None, None, None) == -2     # k > M
+    assert BS(None, None, None, 4, 4, None, None, 8, 2, None, None, None) == -3     # NULL pointers
+    assert BS(None, None, None, 0, 4, None, None, 8, 2, None, None, None) == 0      # no rows

@@ -138,3 +138,42 @@ def test_fused_maxk_layer_chain():
     np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), o_out.view(np.uint32))
     np.testing.assert_array_equal(dsp.cpu().numpy().view(np.uint32), o_dsp.view(np.uint32))
     np.testing.assert_array_equal(dx.cpu().view(torch.int16).numpy().view(np.uint16), o_dx)
+
+
+@pytest.mark.parametrize("M,k,weighted", [(256, 32, True), (512, 64, False), (100, 7, True), (2048, 256, True),
+                                          (8192, 64, True), (36, 4, True)])
+def test_fused_backward_scatter_bit_exact(M, k, weighted):
+    """maxk_sspmm_backward_scatter against the oracle's backward product,
+    rounded to bf16 and scattered (the composition it replaces)."""
+    n_src, n_dst = 1500, 1200
+    _, sp_index = _cbsr(n_src, M, k, seed=41 + M)
+    row_ptr, col, w = synth.power_law_graph(n_dst, n_src, 12.0, seed=42)
+    t_ptr, t_row, t_w = synth.transpose_graph(row_ptr, col, w, n_src)
+    t_w = t_w if weighted else None
+    dout = synth.normal_f32(n_dst, M, seed=43)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = api.maxk_sspmm_backward_scatter(_t(t_ptr), _t(t_row), None if t_w is None else _t(t_w), _t(dout),
+                                          _t(sp_index), M, status=st)
+    torch.cuda.synchronize()
+    want = oracle.sspmm_scatter(t_ptr, t_row, t_w, n_dst, dout, sp_index, M)
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(got.cpu().view(torch.int16).numpy().view(np.uint16), want)
+
+
+def test_fused_backward_scatter_flags_bad_index():
+    n_src, n_dst, M, k = 64, 50, 64, 8
+    _, sp_index = _cbsr(n_src, M, k, seed=51)
+    sp_index = sp_index.copy()
+    sp_index[5, 3] = 300
+    row_ptr, col, w = synth.power_law_graph(n_dst, n_src, 4.0, seed=52)
+    t_ptr, t_row, t_w = synth.transpose_graph(row_ptr, col, w, n_src)
+    dout = synth.normal_f32(n_dst, M, seed=53)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = api.maxk_sspmm_backward_scatter(_t(t_ptr), _t(t_row), _t(t_w), _t(dout), _t(sp_index), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 0x8
+    # every other row is exact (the oracle gets an in-range stand-in for the bad entry)
+    g = got.cpu().view(torch.int16).numpy().view(np.uint16)
+    ok_rows = np.r_[0:5, 6:n_src]
+    want = oracle.sspmm_scatter(t_ptr, t_row, t_w, n_dst, dout, np.where(sp_index == 300, 0, sp_index), M)
+    np.testing.assert_array_equal(g[ok_rows], want[ok_rows])

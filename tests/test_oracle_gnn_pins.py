@@ -94,3 +94,52 @@ def test_power_law_degrees():
     assert deg.min() >= 1 and abs(deg.mean() - 30.0) < 3.0
     assert deg.max() > 10 * deg.mean()  # heavy tail
     np.testing.assert_allclose(np.add.reduceat(w.astype(np.float64), row_ptr[:-1]), 1.0, rtol=1e-5)
+
+
+def test_round_bf16_matches_torch_and_ties(oracle_mod):
+    """The oracle's bf16 rounding against torch's conversion (a library
+    routine), on normal, subnormal and huge values, plus hand-made ties."""
+    torch = pytest.importorskip("torch")
+    x = np.concatenate([synth.normal_f32(16, 256, seed=6).ravel(),
+                        synth.subnormals_f32(4, 256, seed=7).ravel(),
+                        synth.outliers_f32(4, 256, seed=8, mag=3e38).ravel()])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle_mod.round_bf16(x), ref)
+    # exact halfway cases: an even last bit stays, an odd one rounds away
+    ties = np.array([0x3F808000, 0x3F818000, 0xBF808000, 0xBF818000, 0x00008000, 0x00018000],
+                    dtype=np.uint32).view(np.float32)
+    np.testing.assert_array_equal(oracle_mod.round_bf16(ties),
+                                  np.array([0x3F80, 0x3F82, 0xBF80, 0xBF82, 0x0000, 0x0002], dtype=np.uint16))
+
+
+def test_fused_backward_scatter_is_the_composition(oracle_mod):
+    """sspmm_scatter: at sp_index the bf16 rounding of the sampled product,
+    +0 everywhere else -- checked on a graph small enough to sum by hand in
+    float64 (every partial sum here is exact in binary32)."""
+    # 3 source rows, 2 destination rows, M = 6, k = 2
+    sp_index = np.array([[0, 4], [1, 5], [2, 3]], dtype=np.int16)
+    dout = np.arange(12, dtype=np.float32).reshape(2, 6) * np.float32(0.5)  # dout[i, m] = (6 i + m) / 2
+    # transposed graph: source 0 -> dst 0 (w 1), dst 1 (w 2); source 1 -> dst 1 (w 4); source 2 -> none
+    t_ptr = np.array([0, 2, 3, 3], dtype=np.int64)
+    t_row = np.array([0, 1, 1], dtype=np.int32)
+    t_w = np.array([1.0, 2.0, 4.0], dtype=np.float32)
+    g = oracle_mod.sspmm_scatter(t_ptr, t_row, t_w, 2, dout, sp_index, 6)
+    want = np.zeros((3, 6), dtype=np.float64)
+    want[0, 0] = 1 * 0.0 + 2 * 3.0          # dout[0,0], dout[1,0]
+    want[0, 4] = 1 * 2.0 + 2 * 5.0          # dout[0,4], dout[1,4]
+    want[1, 1] = 4 * 3.5
+    want[1, 5] = 4 * 5.5
+    np.testing.assert_array_equal(oracle_mod.widen_bf16(g).astype(np.float64), want)
+    # random case: the composition, and zeros off the kept columns
+    n_src, n_dst, M, k = 300, 200, 64, 8
+    idx = np.stack([np.sort(np.random.default_rng(s).choice(M, k, replace=False)) for s in range(n_src)])
+    idx = idx.astype(np.int16)
+    row_ptr, col, w = synth.power_law_graph(n_dst, n_src, 6.0, seed=5)
+    tp, tr, tw = synth.transpose_graph(row_ptr, col, w, n_src)
+    do = synth.normal_f32(n_dst, M, seed=9)
+    g = oracle_mod.sspmm_scatter(tp, tr, tw, n_dst, do, idx, M)
+    d_sp = oracle_mod.sspmm_cbsr(tp, tr, tw, n_dst, do, idx)
+    np.testing.assert_array_equal(np.take_along_axis(g, idx.astype(np.int64), 1), oracle_mod.round_bf16(d_sp))
+    mask = np.zeros((n_src, M), dtype=bool)
+    np.put_along_axis(mask, idx.astype(np.int64), True, 1)
+    assert np.all(g[~mask] == 0)

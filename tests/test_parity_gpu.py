@@ -288,3 +288,41 @@ def test_bf16_search_stops_once_kept_set_is_final(value_set, M):
         torch.cuda.synchronize()
         ov, oi, _ = oracle.replay(x, k)
         assert_same_selection(fv, fi, ov, oi, what=f"maxk_forward stop {value_set} M={M} k={k}")
+
+
+# ---- exact mode without pass counts: the search may start from a tighter lower end --------
+@pytest.mark.parametrize("value_set", ["normal", "uniform", "int_ties", "all_equal", "outliers", "subnormal"])
+@pytest.mark.parametrize("M", [64, 100, 256, 1024, 3000, 8192, 20000])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_exact_without_pass_counts_is_the_definition(value_set, M, dtype):
+    """rtopk_select in exact mode (no pass counts requested) against the
+    definition of exact top-k, ties to the lowest index, over every kernel
+    family (rows per warp, warp, block, cluster) and the tie-heavy sets."""
+    N = 300 if M <= 8192 else 64
+    x = synth.make(value_set, N, M, seed=M + 7, dtype=dtype)
+    xt = to_dev(x)
+    for k in sorted({1, 5, 16, 32, 33, 64, min(M, 200)}):
+        v, i = api.rtopk_select(xt, k)
+        torch.cuda.synchronize()
+        ov, oi = oracle.sort_topk(x, k)
+        assert_same_selection(v, i, ov, oi, what=f"{value_set} M={M} {dtype} k={k}")
+
+
+# ---- rows beyond the pages' 8192-element limit: one CTA cluster per row -------------------
+@pytest.mark.parametrize("M", [8193, 12000, 16384, 16385, 32768, 40000, 65536])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cluster_rows(M, dtype):
+    N = 150
+    x = synth.make("int_ties" if M % 2 else "normal", N, M, seed=M, dtype=dtype)
+    for k in (1, 64, 1000, M // 2):
+        for m in (-1, 4):
+            _check_full(x, k, m, what=f"cluster M={M} {dtype} k={k} max_iter={m}")
+
+
+@pytest.mark.parametrize("value_set", ["all_equal", "outliers", "uniform"])
+def test_cluster_rows_adversarial(value_set):
+    N, M = 100, 20000
+    x = synth.make(value_set, N, M, seed=5)
+    for k in (3, 256, 5000):
+        _check_full(x, k, what=f"cluster {value_set} k={k}")
+        _check_full(x, k, 0, 1e-3, what=f"cluster {value_set} k={k} eps")
