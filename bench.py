@@ -450,6 +450,38 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
                                   "edges_per_s": E / (t_gf * 1e-3), "bytes": bytes_gf}
     out["maxk_sspmm_backward"] = {"us": t_gb * 1e3, "gbs": bytes_gb / (t_gb * 1e-3) / 1e9,
                                   "edges_per_s": E / (t_gb * 1e-3), "bytes": bytes_gb}
+    # the backward product with the MaxK scatter fused in: dense bf16 gradient
+    # of the MaxK input instead of the n x k intermediate
+    gx = torch.empty((n, M), dtype=torch.bfloat16, device=dev)
+    bws = lambda: api.maxk_sspmm_backward_scatter(g["tp"], g["tr"], g["tw"], agg, si, M, grad=gx)
+    bws()
+    t_gs = timed(bws, reps) / reps
+    bytes_gs = E * (4 + 4 + k * 4) + n * k * 2 + n * M * 2 + (n + 1) * 8
+    # the same gradient unfused: backward product, bf16 rounding (torch), scatter
+    dsp16 = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+    def chain():
+        api.maxk_sspmm_backward(g["tp"], g["tr"], g["tw"], agg, si, d_sp=dsp)
+        dsp16.copy_(dsp)
+        api.maxk_backward_scatter(dsp16, si, M, grad=gx)
+    chain()
+    t_ch = timed(chain, reps) / reps
+    out["maxk_sspmm_backward_scatter"] = {"us": t_gs * 1e3, "gbs": bytes_gs / (t_gs * 1e-3) / 1e9,
+                                          "edges_per_s": E / (t_gs * 1e-3), "bytes": bytes_gs,
+                                          "unfused_chain_us": t_ch * 1e3}
+    del agg, gx, dsp, dsp16, g
+
+    # rows past the pages' 8192-element limit: one CTA cluster per row
+    for Ml, Nl, kl in ((16384, 16384, 256), (65536, 4096, 256)):
+        xl = torch.randn(Nl, Ml, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
+        vl = torch.empty((Nl, kl), dtype=torch.float32, device=dev)
+        il = torch.empty((Nl, kl), dtype=torch.int32, device=dev)
+        f = lambda: api.rtopk_select(xl, kl, vals=vl, idx=il)
+        f()
+        t_l = timed(f, 10) / 10
+        by = Nl * Ml * 4 + Nl * kl * 8
+        out[f"cluster_rows_M{Ml}_k{kl}"] = {"us": t_l * 1e3, "gbs": by / (t_l * 1e-3) / 1e9,
+                                            "rows_per_s": Nl / (t_l * 1e-3), "N": Nl}
+        del xl, vl, il
     return out
 
 

@@ -9,7 +9,8 @@
  *          "Approach" (binary search over the value range for a threshold
  *          selecting k, early stop by capping iterations, second pass filling
  *          borderline ties), "Surprising findings" (precision epsilon),
- *          "Limitations" (M > 8192 unsupported).
+ *          "Limitations" (the method stops at M = 8192; rtopk_select goes on
+ *          to 65536 with one CTA cluster per row, same arithmetic).
  *  [MaxK]  "MaxK-GNN: Extremely Fast GPU Kernel Design for Accelerating Graph
  *          Neural Networks Training": "How MaxK-GNN works" ("The idea": exactly
  *          k survivors per row stored as two dense arrays; "Asymmetric passes,
