@@ -117,14 +117,17 @@ cudaError_t launch_long_rows(const SelectArgs& a, cudaStream_t s) {
   }
 }
 
-// Rows of 8193..65536 elements: one cluster of C CTAs per row, 32 elements
-// per lane (8192 per CTA), C the smallest of 2, 4, 8 that covers the row --
-// the fewer CTAs a row takes, the more rows are in flight at once.
-template <typename T, int C, typename IdxT>
+// Rows of 8193..65536 elements: one cluster of C CTAs per row, NE elements per
+// lane (8 warps x 32 lanes x NE per CTA). The kernel is bound by the latency of
+// its exchange rounds, so what counts is how many rows are in flight: measured
+// on GB300 (fp32, k = 256), rows of 16384 run best as 2 CTAs x 32 elements at 3
+// CTAs per SM (929 us for 2^14 rows), rows of 32768 / 65536 as 2 / 4 CTAs x 64
+// elements (843 / 912 us for 2^13 / 2^12 rows; 1020 / 1250 us with 32 elements).
+template <typename T, int C, int NE, typename IdxT>
 cudaError_t launch_cluster_c(const SelectArgs& a, cudaStream_t s) {
   constexpr int V = ElemTraits<T>::V;
-  constexpr int G = 32 / V;
-  constexpr int kRow = C * kBlockWarps * G * 32 * V;
+  constexpr int G = NE / V;
+  constexpr int kRow = C * kBlockWarps * 32 * NE;
   const bool vec = (a.M % V == 0) && aligned16(a.in);
   const bool full = vec && a.M == kRow;
   const bool exact = a.max_iter < 0 && a.eps == 0.0f;
@@ -150,9 +153,9 @@ cudaError_t launch_cluster_c(const SelectArgs& a, cudaStream_t s) {
 
 template <typename T, typename IdxT>
 cudaError_t launch_cluster_rows(const SelectArgs& a, cudaStream_t s) {
-  if (a.M <= 2 * 8192) return launch_cluster_c<T, 2, IdxT>(a, s);
-  if (a.M <= 4 * 8192) return launch_cluster_c<T, 4, IdxT>(a, s);
-  if (a.M <= 8 * 8192) return launch_cluster_c<T, 8, IdxT>(a, s);
+  if (a.M <= 2 * 8192) return launch_cluster_c<T, 2, 32, IdxT>(a, s);
+  if (a.M <= 2 * 16384) return launch_cluster_c<T, 2, 64, IdxT>(a, s);
+  if (a.M <= 4 * 16384) return launch_cluster_c<T, 4, 64, IdxT>(a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -137,6 +137,25 @@ __device__ __forceinline__ int group_max_floor(float mx, int k) {
   return __reduce_min_sync(0xffffffffu, f2o(mx));
 }
 
+// Counts of this lane's x below three thresholds in one sweep (same rule as
+// lane_count_lt for each).
+template <int G, int V>
+__device__ __forceinline__ void lane_count_lt3(const float (&x)[G][V], float m1, float m2, float m3,
+                                               unsigned& c1, unsigned& c2, unsigned& c3) {
+  const float t1 = (m1 == 0.0f) ? -0.0f : m1;
+  const float t2 = (m2 == 0.0f) ? -0.0f : m2;
+  const float t3 = (m3 == 0.0f) ? -0.0f : m3;
+  c1 = 0u; c2 = 0u; c3 = 0u;
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      c1 += __float_as_uint(__fsub_rn(x[g][e], t1)) >> 31;
+      c2 += __float_as_uint(__fsub_rn(x[g][e], t2)) >> 31;
+      c3 += __float_as_uint(__fsub_rn(x[g][e], t3)) >> 31;
+    }
+}
+
 // True when [lo, hi) holds at most one bf16 value (lo <= hi finite). For bf16
 // data every count c(t) only changes at bf16 values, so from then on further
 // passes move lo and hi without changing S = {x >= hi} or B = {lo <= x < hi}:
