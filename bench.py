@@ -485,6 +485,46 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
     return out
 
 
+def _case_cluster():
+    # rows past the pages' limit: 1024 rows of 65536 fp32 N(0,1), k = 256 (268 MB in)
+    import torch
+    from maxk_sparse_activations_gb300 import api
+    dev = torch.device("cuda")
+    x = torch.randn(1024, 65536, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
+    v = torch.empty((1024, 256), device=dev)
+    i = torch.empty((1024, 256), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        api.rtopk_select(x, 256, vals=v, idx=i)
+
+
+def _case_fused_backward():
+    # the aggregation graph of the secondary measurements (2^17 nodes, mean
+    # in-degree 64, power-law tail), M = 256, k = 32: fused backward + scatter
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    n, M, k = 1 << 17, 256, 32
+    xb = torch.from_numpy(synth.normal_bf16(n, M, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    _, fi = api.maxk_forward(xb, k)
+    row_ptr, col, w = synth.power_law_graph(n, n, 64.0, seed=5, alpha=2.5, max_degree=4096)
+    t_ptr, t_row, t_w = synth.transpose_graph(row_ptr, col, w, n)
+    tp, tr, tw = (torch.from_numpy(a).to(dev) for a in (t_ptr, t_row, t_w))
+    dout = torch.randn(n, M, device=dev)
+    gx = torch.empty((n, M), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        api.maxk_sspmm_backward_scatter(tp, tr, tw, dout, fi, M, grad=gx)
+
+
+PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward}
+
+
+def run_case(name: str) -> int:
+    import torch
+    PROFILE_CASES[name]()
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     global N_ROWS
     ap = argparse.ArgumentParser()
@@ -496,8 +536,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=N_ROWS,
                     help="rows per rank (default 2^20, the metric's workload; smaller only for profiling)")
+    ap.add_argument("--case", choices=sorted(PROFILE_CASES),
+                    help="run three launches of one secondary kernel on its workload and exit "
+                         "(a small, self-contained target for profiler captures; prints no JSON)")
     args = ap.parse_args()
     N_ROWS = args.rows
+    if args.case:
+        return run_case(args.case)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:
