@@ -85,7 +85,8 @@ typedef enum {
   RTOPK_EINVAL_PTR = -3,   /* a required pointer is NULL (with N > 0) */
   RTOPK_EINVAL_DTYPE = -4, /* dtype is not an rtopk_dtype value */
   RTOPK_ECUDA = -5,        /* a CUDA runtime call or launch failed */
-  RTOPK_EINVAL_ARG = -6    /* eps < 0 or NaN; buckets not dividing M and k */
+  RTOPK_EINVAL_ARG = -6,   /* eps < 0 or NaN; buckets not dividing M and k */
+  RTOPK_EDEVICE = -7       /* rtopk_status_read: the device status word is non-zero */
 } rtopk_status;
 
 /*
@@ -237,6 +238,19 @@ int maxk_sspmm_backward(const int64_t* t_row_ptr, const int32_t* t_dst, const fl
 int maxk_sspmm_backward_scatter(const int64_t* t_row_ptr, const int32_t* t_dst, const float* t_edge_w,
                                 int64_t n_src, int64_t n_dst, const float* dout, const int16_t* sp_index,
                                 int32_t M, int32_t k, void* grad_bf16, uint32_t* status, cudaStream_t stream);
+
+/*
+ * rtopk_status_read -- read a device status word after the work that sets it.
+ * Waits for `stream`, copies the word to the host and returns RTOPK_EDEVICE if
+ * any RTOPK_STATUS_* bit is set, else RTOPK_OK (RTOPK_ECUDA if the copy or the
+ * wait fails). The pages define no error reporting; this is the host side of
+ * the status words the entry points above fill.
+ *
+ *  status  the word passed as `status` to the earlier calls (device or pinned host memory)
+ *  bits    host uint32 or NULL: receives the word
+ * Blocks the calling thread until `stream` has drained; allocates nothing.
+ */
+int rtopk_status_read(const uint32_t* status, uint32_t* bits, cudaStream_t stream);
 
 /* Human-readable text for an rtopk_status code (static storage, never NULL). */
 const char* rtopk_strerror(int code);

@@ -6,6 +6,7 @@ that the input generators and host-side reporting import without a GPU.
 """
 
 __all__ = ["rtopk_select", "rtopk_select_stats", "rtopk_select_bucketed", "maxk_forward", "maxk_backward_scatter", "MaxK",
+           "read_status",
            "maxk_spgemm_forward", "maxk_sspmm_backward", "maxk_sspmm_backward_scatter"]
 
 

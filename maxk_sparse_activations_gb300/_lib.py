@@ -24,8 +24,8 @@ STATUS_BAD_EDGE = 0x10
 
 #: every symbol include/rtopk.h declares
 EXPORTED = ("rtopk_select", "rtopk_select_stats", "rtopk_select_bucketed", "maxk_forward", "maxk_backward_scatter",
-            "maxk_spgemm_forward", "maxk_sspmm_backward", "maxk_sspmm_backward_scatter", "rtopk_strerror",
-            "rtopk_version")
+            "maxk_spgemm_forward", "maxk_sspmm_backward", "maxk_sspmm_backward_scatter", "rtopk_status_read",
+            "rtopk_strerror", "rtopk_version")
 
 
 def load(build_if_stale: bool = True) -> ctypes.CDLL:
@@ -52,6 +52,8 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
         lib.maxk_spgemm_forward.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p, p, p]
         lib.maxk_sspmm_backward.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p, p, p]
         lib.maxk_sspmm_backward_scatter.argtypes = [p, p, p, i64, i64, p, p, i32, i32, p, p, p]
+        lib.rtopk_status_read.argtypes = [p, p, p]
+        lib.rtopk_status_read.restype = ctypes.c_int
         lib.rtopk_strerror.argtypes = [ctypes.c_int]
         lib.rtopk_strerror.restype = ctypes.c_char_p
         lib.rtopk_version.argtypes = []

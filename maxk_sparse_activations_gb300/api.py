@@ -9,6 +9,8 @@ read and write the host buffers directly over NVLink-C2C, with no staging copy.
 """
 from __future__ import annotations
 
+import ctypes
+
 from typing import Optional
 
 import torch
@@ -258,3 +260,16 @@ def maxk_sspmm_backward_scatter(t_row_ptr: torch.Tensor, t_dst: torch.Tensor, t_
                                                  grad.data_ptr(), _ptr(status), _stream_ptr(stream, dout.device))
     _lib.check(rc, "maxk_sspmm_backward_scatter")
     return grad
+
+
+def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Waits for the stream and returns the device status word's bits
+    (0 = every row valid; see the RTOPK_STATUS_* bits in include/rtopk.h)."""
+    if status.numel() != 1 or status.element_size() != 4:
+        raise ValueError("status must be a one-element 32-bit tensor")
+    bits = ctypes.c_uint32(0)
+    dev = status.device if status.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    rc = _lib.load().rtopk_status_read(status.data_ptr(), ctypes.addressof(bits), _stream_ptr(stream, dev))
+    if rc not in (0, -7):
+        _lib.check(rc, "rtopk_status_read")
+    return int(bits.value)

@@ -107,6 +107,15 @@ int maxk_sspmm_backward_scatter(const int64_t* t_row_ptr, const int32_t* t_dst, 
                                            nullptr, static_cast<uint16_t*>(grad_bf16), status, stream));
 }
 
+int rtopk_status_read(const uint32_t* status, uint32_t* bits, cudaStream_t stream) {
+  if (status == nullptr) return RTOPK_EINVAL_PTR;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, status, sizeof(word), cudaMemcpyDefault, stream) != cudaSuccess) return RTOPK_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return RTOPK_ECUDA;
+  if (bits != nullptr) *bits = word;
+  return word == 0u ? RTOPK_OK : RTOPK_EDEVICE;
+}
+
 const char* rtopk_strerror(int code) {
   switch (code) {
     case RTOPK_OK: return "ok";
@@ -116,6 +125,7 @@ const char* rtopk_strerror(int code) {
     case RTOPK_EINVAL_PTR: return "a required device pointer is NULL";
     case RTOPK_EINVAL_DTYPE: return "unknown dtype: use RTOPK_F32 or RTOPK_BF16";
     case RTOPK_ECUDA: return "a CUDA runtime call or kernel launch failed";
+    case RTOPK_EDEVICE: return "the device status word reports invalid rows, a safety cap or bad indices";
     case RTOPK_EINVAL_ARG: return "invalid argument: need eps >= 0, and buckets dividing both M and k";
     default: return "unknown rtopk status code";
   }

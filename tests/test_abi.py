@@ -86,3 +86,10 @@ def test_argument_errors_launch_nothing(lib):
     assert BS(None, None, None, 4, 4, None, None, 8, 9, None, None, None) == -2     # k > M
     assert BS(None, None, None, 4, 4, None, None, 8, 2, None, None, None) == -3     # NULL pointers
     assert BS(None, None, None, 0, 4, None, None, 8, 2, None, None, None) == 0      # no rows
+
+
+def test_status_read_arguments(lib):
+    # a NULL word is an argument error, returned before any CUDA call
+    assert lib.rtopk_status_read(None, None, None) == -3
+    from maxk_sparse_activations_gb300 import _lib
+    assert "status word" in _lib.strerror(-7)

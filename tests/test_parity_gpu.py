@@ -193,6 +193,14 @@ def test_status_word_flags_bad_rows():
     x[20, 5] = np.float32(3e38)
     v, i, it, st = _run(x, 32)
     assert st & 0x1 and st & 0x2 and not st & 0x4
+    # the host reader returns the same bits (RTOPK_EDEVICE underneath)
+    xt = to_dev(x)
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.rtopk_select_stats(xt, 32, status=word)
+    assert api.read_status(word) == st
+    clean = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.rtopk_select_stats(to_dev(synth.normal_f32(64, 256, seed=1)), 32, status=clean)
+    assert api.read_status(clean) == 0
     good = np.setdiff1d(np.arange(64), [3, 9, 20])
     ov, oi, _ = oracle.replay(x[good], 32)
     assert_same_selection(v, i, ov, oi, rows=good, what="good rows beside bad ones")
