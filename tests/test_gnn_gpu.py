@@ -177,3 +177,27 @@ def test_fused_backward_scatter_flags_bad_index():
     ok_rows = np.r_[0:5, 6:n_src]
     want = oracle.sspmm_scatter(t_ptr, t_row, t_w, n_dst, dout, np.where(sp_index == 300, 0, sp_index), M)
     np.testing.assert_array_equal(g[ok_rows], want[ok_rows])
+
+
+def test_fused_backward_scatter_flags_bad_edge():
+    n_src, n_dst, M, k = 60, 40, 64, 8
+    _, sp_index = _cbsr(n_src, M, k, seed=61)
+    row_ptr, col, w = synth.power_law_graph(n_dst, n_src, 4.0, seed=62)
+    t_ptr, t_row, t_w = synth.transpose_graph(row_ptr, col, w, n_src)
+    t_row = t_row.copy()
+    t_row[0] = n_dst + 3  # destination out of range: skipped and flagged
+    dout = synth.normal_f32(n_dst, M, seed=63)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = api.maxk_sspmm_backward_scatter(_t(t_ptr), _t(t_row), _t(t_w), _t(dout), _t(sp_index), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 0x10
+    # the source row owning edge 0 sums its other edges; every other row is exact
+    src0 = int(np.searchsorted(t_ptr, 0, side="right") - 1)
+    keep = np.ones(t_row.shape[0], dtype=bool)
+    keep[0] = False
+    deg = np.diff(t_ptr)
+    deg[src0] -= 1
+    t_ptr2 = np.zeros_like(t_ptr)
+    np.cumsum(deg, out=t_ptr2[1:])
+    want = oracle.sspmm_scatter(t_ptr2, t_row[keep], t_w[keep], n_dst, dout, sp_index, M)
+    np.testing.assert_array_equal(got.cpu().view(torch.int16).numpy().view(np.uint16), want)

@@ -334,3 +334,19 @@ def test_cluster_rows_adversarial(value_set):
     for k in (3, 256, 5000):
         _check_full(x, k, what=f"cluster {value_set} k={k}")
         _check_full(x, k, 0, 1e-3, what=f"cluster {value_set} k={k} eps")
+
+
+def test_cluster_rows_status_and_neighbours():
+    """Non-finite and out-of-range rows in the cluster path set their status
+    bits and leave the other rows of the same launch exact."""
+    N, M, k = 24, 20000, 100
+    x = synth.normal_f32(N, M, seed=9)
+    x[2, 17] = np.nan
+    x[7, 19999] = -np.inf
+    x[11, 4000] = np.float32(2e38)
+    v, i, it, st = _run(x, k)
+    assert st & 0x1 and st & 0x2 and not st & 0x4
+    good = np.setdiff1d(np.arange(N), [2, 7, 11])
+    ov, oi, oit = oracle.replay(x[good], k)
+    assert_same_selection(v, i, ov, oi, rows=good, what="cluster good rows beside bad ones")
+    np.testing.assert_array_equal(it[good], oit)
