@@ -48,7 +48,7 @@ def algorithmic_bytes(N, M, k, s_in, s_val, s_idx):
 
 # sources that define the timed kernel (fp32 rows of <= 2048 elements, one warp per row)
 # and its launch configuration
-HEADLINE_SOURCES = ("rtopk_device.cuh", "rtopk_select.cuh", "rtopk_warp.cuh", "rtopk_block.cuh",
+HEADLINE_SOURCES = ("rtopk_device.cuh", "rtopk_select.cuh", "rtopk_warp.cuh", "rtopk_packed.cuh", "rtopk_block.cuh",
                     "rtopk_dispatch.cuh", "rtopk_f32.cu", "launch_util.cu")
 
 
@@ -338,7 +338,7 @@ def run_gb300(args, rank: int, world: int):
                          "frac": gbs / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                          else "fallback", "algorithmic_bytes_per_launch": bytes_step,
-                         "kernel": "rtopk_warp_kernel<float,G=2,EXACT,L=0,int32>",
+                         "kernel": "rtopk_warp_packed_kernel<float,G=2,int32>",
                          "traffic_source": os.path.relpath(prof, ROOT) if prof else None},
             "cpu_baseline": cpu,
             "e2e": {"value": world * N_ROWS / (ms_e2e * 1e-3), "unit": "rows/s",
@@ -366,6 +366,13 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
         f = lambda: api.rtopk_select(x, k, m, 0.0, vals=vals, idx=idx)
         f()
         out[f"rtopk_f32_max_iter_{m}_us"] = timed(f, reps) / reps * 1e3
+    # exact mode with per-row pass counts: the binary32 replay kernel (the packed
+    # 16-bit search runs only when pass counts are not requested)
+    iters_buf = torch.empty((N,), dtype=torch.int32, device=dev)
+    st_buf = torch.zeros((1,), dtype=torch.int32, device=dev)
+    f = lambda: api.rtopk_select_stats(x, k, vals=vals, idx=idx, iters=iters_buf, status=st_buf)
+    f()
+    out["rtopk_f32_exact_binary32_with_pass_counts_us"] = timed(f, reps) / reps * 1e3
     # context: PyTorch's own row-wise topk on the same matrix (the baseline the RTop-K
     # page reports its 7.29x exact / 11.49x max_iter=2 kernel speedups against)
     f = lambda: torch.topk(x, k, dim=1, largest=True, sorted=True)

@@ -5,6 +5,7 @@
 #include "rtopk_select.cuh"
 #include "rtopk_block.cuh"
 #include "rtopk_cluster.cuh"
+#include "rtopk_packed.cuh"
 
 namespace rtopk {
 
@@ -20,6 +21,18 @@ cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s
   constexpr int kThreads = 256;
   constexpr int NE = G * ElemTraits<T>::V;
   const bool exact = a.max_iter < 0 && a.eps == 0.0f;
+  if constexpr (NE <= 16) {
+    // exact mode without pass counts on full rows: the search counts on packed
+    // 16-bit images of the row (rtopk_packed.cuh)
+    if (exact && a.iters == nullptr && full && a.k <= kStageK) {
+      auto pk = rtopk_warp_packed_kernel<T, G, IdxT>;
+      const int blocks = persistent_blocks(reinterpret_cast<const void*>(pk), kThreads, 0, (a.N + 7) / 8);
+      if (blocks <= 0) return cudaErrorInvalidConfiguration;
+      pk<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, static_cast<T*>(a.vals),
+                                     static_cast<IdxT*>(a.idx), a.status);
+      return cudaGetLastError();
+    }
+  }
   const int L = (NE >= 64 && a.k <= 128) ? 8 : ((NE >= 32 && a.k <= 64) ? 4 : 0);
   using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);
   K kern;

@@ -1,0 +1,334 @@
+// Exact row-wise top-k, one warp per row, with the threshold search counted on
+// packed 16-bit images of the row (two elements per instruction), sm_103a.
+//
+// Source: "RTop-K: Ultra-Fast Row-Wise Top-K Selection for Neural Network
+// Acceleration on GPUs" (summary page), "Approach" (binary search over the
+// row's value range for a threshold that selects k; ties at the threshold
+// filled by the lowest index); CBSR output from "MaxK-GNN: Extremely Fast GPU
+// Kernel Design for Accelerating Graph Neural Networks Training", "The idea".
+//
+// Used for exact mode (max_iter < 0, eps == 0) when per-row pass counts are
+// not requested. The result there is one set -- the k largest values, ties at
+// the k-th value broken by the lowest index -- whatever thresholds the
+// bisection visits, so the search may run on any order-preserving image of the
+// row. Here the image h(x) is 16 bits wide:
+//  * bf16 rows: the data themselves (h(x) = x, counts exact);
+//  * fp32 rows: binary16 rounded to nearest, saturated at +-65504. Rounding is
+//    monotone (x <= y implies h(x) <= h(y)), so for any 16-bit threshold t the
+//    set {h(x) >= t} is an upper set of the row in value order.
+// One pass counts C(t) = #{h(x) >= t} with one packed compare (set.ge.*x2,
+// 1.0 or 0.0 per half) and one packed add per two elements, instead of two
+// instructions per element on binary32. The coarse bisection keeps
+// C(lo) >= k > C(hi) on 16-bit values lo < hi:
+//  * C(mid) == k: {h(x) >= mid} has exactly k members and is an upper set, so
+//    it is the exact top-k (two equal values have equal images: no tie at the
+//    k-th value can straddle it). Stored straight from the packed compares.
+//  * no 16-bit value strictly inside (lo, hi): A = {h(x) >= hi} (|A| < k) is
+//    kept, everything below lo is dropped, and the rest of the top-k lies in
+//    the bucket B = {lo <= h(x) < hi}, all of whose values are below A's and
+//    above the dropped ones. The binary32 search then finishes from
+//    [min B, next binary32 above max B], a valid bracket (c(min B) >= k,
+//    c(above max B) = |A| < k), and the general fill writes the row. For bf16
+//    rows lo and hi are adjacent, B holds one value, and the fill runs at once.
+// Rows whose values are not all finite with |x| <= 1e38 take the binary32
+// kernel's path (status bits, bounded search).
+//
+// Counting detail: the per-lane accumulator starts at 1024.0 (binary16) or
+// 128.0 (bf16) in both halves, where the spacing is 1, so adding 1.0 per kept
+// element is exact and the field bits read (magic + count). One integer
+// multiply-add folds the two halves into bits 16..31 and removes the offsets,
+// and one redux.sync sums the lanes.
+#pragma once
+
+#include "rtopk_warp.cuh"
+
+namespace rtopk {
+
+template <typename T>
+struct Packed16;
+
+// fp32 rows: binary16 image
+template <>
+struct Packed16<float> {
+  static constexpr uint32_t kMagic2 = 0x64006400u;  // 1024.0 in both halves
+  static constexpr uint32_t kFold = 0xc8006400u;     // (2 * 0x6400 << 16) + 0x6400
+  static constexpr uint32_t kInf2 = 0x7c007c00u;     // +inf in both halves
+  // both halves = round-to-nearest binary16 of v, saturated at +-65504
+  static __device__ __forceinline__ uint32_t splat(float v) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(v));
+    return d;
+  }
+  // the pair (hi element, lo element) -> one word (lo element in bits 0..15)
+  static __device__ __forceinline__ uint32_t pack(float hi_elem, float lo_elem) {
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi_elem), "f"(lo_elem));
+    return d;
+  }
+  static __device__ __forceinline__ float low_f32(uint32_t w) {
+    float f;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
+    return f;
+  }
+  static __device__ __forceinline__ float high_f32(uint32_t w) {
+    float f;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, u;\n\t}" : "=f"(f) : "r"(w));
+    return f;
+  }
+  static __device__ __forceinline__ uint32_t set_ge(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("set.ge.f16x2.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+};
+
+// bf16 rows: the data themselves
+template <>
+struct Packed16<uint16_t> {
+  static constexpr uint32_t kMagic2 = 0x43004300u;  // 128.0 in both halves
+  static constexpr uint32_t kFold = 0x86004300u;     // (2 * 0x4300 << 16) + 0x4300
+  static constexpr uint32_t kInf2 = 0x7f807f80u;
+  static __device__ __forceinline__ uint32_t splat(float v) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(v));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t pack(float hi_elem, float lo_elem) {
+    return (__float_as_uint(hi_elem) & 0xffff0000u) | (__float_as_uint(lo_elem) >> 16);  // exact: bf16 data
+  }
+  static __device__ __forceinline__ float low_f32(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float high_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+  static __device__ __forceinline__ uint32_t set_ge(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("set.ge.bf16x2.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+};
+
+// Number of this lane's packed elements with h >= t in words [w0, w0 + n),
+// shifted into bits 16..31 (low bits hold junk below 2^16).
+template <typename P, int NW>
+__device__ __forceinline__ uint32_t packed_count_hi16(const uint32_t (&h)[NW], int w0, int n, uint32_t t2) {
+  uint32_t acc = P::add(P::kMagic2, P::set_ge(h[w0], t2));
+#pragma unroll
+  for (int q = 1; q < n; ++q) acc = P::add(acc, P::set_ge(h[w0 + q], t2));
+  return acc * 0x10001u - P::kFold;  // (c_hi + c_lo) << 16 | c_lo
+}
+
+// Smallest binary32 above v (v finite).
+__device__ __forceinline__ float next_up_f32(float v) {
+  const int b = __float_as_int(v);
+  if ((b & 0x7fffffff) == 0) return __int_as_float(1);
+  return __int_as_float(b >= 0 ? b + 1 : b - 1);
+}
+
+// Smallest bf16 above v (v a finite bf16 value widened to binary32).
+__device__ __forceinline__ float next_up_bf16(float v) {
+  const uint32_t b = __float_as_uint(v);
+  if ((b & 0x7fffffffu) == 0u) return __uint_as_float(0x10000u);
+  return __uint_as_float((b & 0x80000000u) ? b - 0x10000u : b + 0x10000u);
+}
+
+// Writes the elements with h >= t2 (exactly `k` of them, an upper set of the
+// row) in ascending index order to stage[0 .. k).
+template <typename T, int G>
+__device__ __forceinline__ void compact_packed(const float (&x)[G][ElemTraits<T>::V],
+                                               const uint32_t (&h)[G * ElemTraits<T>::V / 2], uint32_t t2,
+                                               int k, int lane, float2* __restrict__ stage) {
+  using P = Packed16<T>;
+  constexpr int V = ElemTraits<T>::V;
+  constexpr int WG = V / 2;  // words per group
+  constexpr int GS = 32 * V;
+  constexpr int FB = (GS <= 255) ? 8 : 16;
+  constexpr int FPW = 32 / FB;
+  constexpr unsigned FMASK = (1u << FB) - 1u;
+  constexpr int NWF = (G + FPW - 1) / FPW;
+  uint32_t s[G][WG];
+  unsigned pkw[NWF];
+#pragma unroll
+  for (int q = 0; q < NWF; ++q) pkw[q] = 0u;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    uint32_t acc = P::kMagic2;
+#pragma unroll
+    for (int q = 0; q < WG; ++q) {
+      s[g][q] = P::set_ge(h[g * WG + q], t2);
+      acc = P::add(acc, s[g][q]);
+    }
+    const unsigned c = (acc * 0x10001u - P::kFold) >> 16;
+    pkw[g / FPW] += c << (FB * (g % FPW));
+  }
+  const int jl = lane * V;
+  int base = 0;
+#pragma unroll
+  for (int q = 0; q < NWF; ++q) {
+    unsigned tot;
+    const unsigned ex = warp_excl_scan(pkw[q], lane, tot);
+#pragma unroll
+    for (int f = 0; f < FPW; ++f) {
+      const int g = q * FPW + f;
+      if (g < G) {
+        int pos = base + int((ex >> (FB * f)) & FMASK);
+#pragma unroll
+        for (int w = 0; w < WG; ++w) {
+          // (pos < k holds whenever exactly k elements pass; the test keeps every
+          // store inside the staging row regardless)
+          if ((s[g][w] & 0xffffu) && pos < k) {
+            stage[pos] = make_float2(x[g][2 * w], __int_as_float(g * GS + jl + 2 * w));
+            ++pos;
+          }
+          if ((s[g][w] >> 16) && pos < k) {
+            stage[pos] = make_float2(x[g][2 * w + 1], __int_as_float(g * GS + jl + 2 * w + 1));
+            ++pos;
+          }
+        }
+        base += int((tot >> (FB * f)) & FMASK);
+      }
+    }
+  }
+}
+
+template <typename T, int G, typename IdxT>
+__device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTraits<T>::V], int64_t r, int M, int k,
+                                                   int lane, float2* __restrict__ stage, T* __restrict__ vals,
+                                                   IdxT* __restrict__ idx, uint32_t& st) {
+  using P = Packed16<T>;
+  constexpr int V = ElemTraits<T>::V;
+  constexpr int NE = G * V;
+  constexpr int NW = NE / 2;
+  constexpr unsigned FULL = 0xffffffffu;
+
+  // ---- value range (binary32, NaN-propagating) and the precondition
+  float mx = neg_inf(), mn = pos_inf();
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      mx = max_nan(mx, x[g][e]);
+      mn = min_nan(mn, x[g][e]);
+    }
+  const float hi32 = o2f(__reduce_max_sync(FULL, f2o(mx)));
+  const float lo32 = o2f(__reduce_min_sync(FULL, f2o(mn)));
+  if (!(lo32 >= -1e38f && hi32 <= 1e38f)) {
+    // invalid row: the binary32 path flags it and keeps every write in the row
+    process_row_w1<T, G, true, 0, IdxT>(x, true, r, M, k, kSafetyCap, true, 0.0f, lane, stage, vals, idx,
+                                        nullptr, st);
+    return;
+  }
+
+  // ---- packed image: word w of group g holds elements 2w (bits 0..15) and 2w + 1
+  uint32_t h[NW];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int w = 0; w < V / 2; ++w) h[g * (V / 2) + w] = P::pack(x[g][2 * w + 1], x[g][2 * w]);
+  auto count = [&](uint32_t t2) { return int(__reduce_add_sync(FULL, packed_count_hi16<P, NW>(h, 0, NW, t2)) >> 16); };
+
+  // ---- coarse bracket: hi = image of the maximum; lo = image of the minimum,
+  // or, for k <= 32, of the smallest lane maximum (each of the 32 lanes holds an
+  // element at least that large, so C(lo) >= 32 >= k)
+  const uint32_t hi2 = P::splat(hi32);
+  float hi = P::low_f32(hi2);
+  const float lo_src = (k <= 32) ? o2f(__reduce_min_sync(FULL, f2o(mx))) : lo32;
+  float lo = P::low_f32(P::splat(lo_src));
+
+  float b_lo, b_hi;  // coarse bucket [b_lo, b_hi) that the binary32 search finishes
+  // ties at the top image: only possible when enough lanes' maxima share it
+  if (__popc(__ballot_sync(FULL, P::low_f32(P::splat(mx)) >= hi)) * NE >= k && count(hi2) >= k) {
+    b_lo = hi;
+    b_hi = pos_inf();
+  } else {
+    bool eq = false;
+    uint32_t t2 = 0u;
+    for (;;) {
+      const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
+      t2 = P::splat(mid);
+      const float m = P::low_f32(t2);
+      if (!(lo < m && m < hi)) break;  // no 16-bit value strictly inside
+      const int cnt = count(t2);
+      if (cnt == k) { eq = true; break; }
+      const bool ge = cnt > k;
+      lo = ge ? m : lo;
+      hi = ge ? hi : m;
+    }
+    const int64_t obase = r * int64_t(k);
+    if (eq) {
+      compact_packed<T, G>(x, h, t2, k, lane, stage);
+      __syncwarp();
+      for (int p = lane; p < k; p += 32) {
+        const float2 e = stage[p];
+        vals[obase + p] = out_value(e.x, vals);
+        idx[obase + p] = IdxT(__float_as_int(e.y));
+      }
+      __syncwarp();
+      return;
+    }
+    if (sizeof(T) == 2 && next_up_bf16(lo) == hi) {
+      // bf16 rows: B = {x == lo}, all tied; keep x >= hi and fill from B by index
+      fill_store_w1<T, G, IdxT>(x, lo, hi, false, k, lane, stage, vals, idx, obase);
+      return;
+    }
+    b_lo = lo;
+    b_hi = hi;
+  }
+
+  // ---- binary32 search inside the bucket B = {b_lo <= h(x) < b_hi}
+  float bmin = pos_inf(), bmax = neg_inf();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const float hl = P::low_f32(h[w]), hh = P::high_f32(h[w]);
+    const float xl = x[w / (V / 2)][2 * (w % (V / 2))], xh = x[w / (V / 2)][2 * (w % (V / 2)) + 1];
+    const bool il = hl >= b_lo && !(hl >= b_hi);
+    const bool ih = hh >= b_lo && !(hh >= b_hi);
+    bmin = fminf(bmin, il ? xl : pos_inf());
+    bmax = fmaxf(bmax, il ? xl : neg_inf());
+    bmin = fminf(bmin, ih ? xh : pos_inf());
+    bmax = fmaxf(bmax, ih ? xh : neg_inf());
+  }
+  float flo = o2f(__reduce_min_sync(FULL, f2o(bmin)));
+  float fhi = next_up_f32(o2f(__reduce_max_sync(FULL, f2o(bmax))));
+  int it = 0, c_lo = M;
+  bool comp = false;
+  auto count_row = [&](float mid) { return __reduce_add_sync(FULL, lane_count_lt<G, V>(x, mid)); };
+  const bool eq32 = search_passes<true, 0>(count_row, 32 * NE, k, kSafetyCap, true, 0.0f, flo, fhi, it, c_lo,
+                                           comp, st);
+  fill_store_w1<T, G, IdxT>(x, flo, fhi, eq32, k, lane, stage, vals, idx, r * int64_t(k));
+}
+
+// Minimum resident blocks per SM of the packed kernel.
+template <int NE>
+struct PackedOcc {
+  static constexpr int value = NE <= 8 ? 5 : 3;
+};
+
+// Rows of exactly G * 32 * V elements, 16-byte aligned, exact mode, k <= kStageK.
+template <typename T, int G, typename IdxT>
+__global__ void __launch_bounds__(256, PackedOcc<G * ElemTraits<T>::V>::value)
+rtopk_warp_packed_kernel(const T* __restrict__ in, int64_t N, int M, int k, T* __restrict__ vals,
+                         IdxT* __restrict__ idx, uint32_t* __restrict__ status) {
+  constexpr int V = ElemTraits<T>::V;
+  __shared__ float2 stage_all[8][kStageK];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  float2* stage = stage_all[wib];
+  const int64_t nwarps = int64_t(gridDim.x) * 8;
+  uint32_t st = 0;
+  for (int64_t r = int64_t(blockIdx.x) * 8 + wib; r < N; r += nwarps) {
+    float x[G][V];
+    load_row<G, 1, true>(in + r * int64_t(M), M, 0, lane, true, x);
+    process_row_packed<T, G, IdxT>(x, r, M, k, lane, stage, vals, idx, st);
+  }
+  if (status != nullptr && st != 0u && lane == 0) atomicOr(status, st);
+}
+
+}  // namespace rtopk

@@ -313,71 +313,22 @@ __device__ __forceinline__ void finish_from_list(const float2* __restrict__ list
   }
 }
 
-template <typename T, int G, bool EXACT, int L, typename IdxT>
-__device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>::V], bool full, int64_t r,
-                                               int M, int k, int limit, bool cap_is_safety, float eps, int lane,
-                                               float2* __restrict__ stage, T* __restrict__ vals,
-                                               IdxT* __restrict__ idx, int* __restrict__ iters, uint32_t& st) {
+// Fill pass and CBSR store of one row from the final bracket [lo, hi). With
+// `exact_end` (the search ended on c(lo) == k) the kept set is exactly
+// {x >= lo}; otherwise S = {x >= hi} is kept and B = {lo <= x < hi} fills the
+// remaining k - |S| in ascending index order. Rows with k <= kStageK are
+// staged in shared memory and written out coalesced.
+template <typename T, int G, typename IdxT>
+__device__ __forceinline__ void fill_store_w1(const float (&x)[G][ElemTraits<T>::V], float lo, float hi,
+                                              bool exact_end, int k, int lane, float2* __restrict__ stage,
+                                              T* __restrict__ vals, IdxT* __restrict__ idx, int64_t obase) {
   constexpr int V = ElemTraits<T>::V;
   constexpr int GS = 32 * V;
-  constexpr int NE = G * V;
   constexpr int FB = (GS <= 255) ? 8 : 16;
   constexpr int FPW = 32 / FB;
   constexpr unsigned FMASK = (1u << FB) - 1u;
-
-  // ---- value range (NaN-propagating; pads excluded from the minimum)
-  float mx = neg_inf(), mn = pos_inf();
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      mx = max_nan(mx, x[g][e]);
-      mn = min_nan(mn, (full || g * GS + lane * V + e < M) ? x[g][e] : pos_inf());
-    }
-  float hi = o2f(__reduce_max_sync(0xffffffffu, f2o(mx)));
-  float lo = o2f(__reduce_min_sync(0xffffffffu, f2o(mn)));
-  const bool ok = (lo >= -1e38f && hi <= 1e38f);
-  if (!ok) st |= (isfinite(lo) && isfinite(hi)) ? kStatusRange : kStatusNonFinite;
-
-  // ---- ties at the maximum: only possible if enough lanes hold the maximum
-  bool max_tie = false;
-  if (__popc(__ballot_sync(0xffffffffu, mx == hi)) * NE >= k) {
-    int c = 0;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < V; ++e) c += (x[g][e] >= hi) ? 1 : 0;
-    max_tie = int(__reduce_add_sync(0xffffffffu, unsigned(c))) >= k;
-  }
-
-  int it = 0;
-  bool eq = false, comp = false;
-  int c_lo = M;
-  if (max_tie) {
-    lo = hi;           // keep the k lowest-index maxima through the fill rule:
-    hi = pos_inf();    // S is empty and every maximum is borderline
-  } else {
-    auto count_row = [&](float mid) { return __reduce_add_sync(0xffffffffu, lane_count_lt<G, V>(x, mid)); };
-    eq = search_passes<EXACT, L, decltype(count_row), (V == 8)>(count_row, 32 * NE, k, limit, cap_is_safety,
-                                                                 eps, lo, hi, it, c_lo, comp, st, iters == nullptr);
-  }
-  comp = comp && ok;
-
-  const int64_t obase = r * int64_t(k);
   const bool staged = (k <= kStageK);
-  if (L > 0 && comp) {
-    // ---- compacted phase: list of the c(lo) <= 32 L elements >= lo
-    compact_ge<G, V>(x, lo, lane, stage);
-    __syncwarp();
-    finish_from_list<EXACT, (L > 0 ? L : 1), T, IdxT>(stage, c_lo, lo, hi, it, k, limit, cap_is_safety, eps,
-                                                     lane, vals, idx, obase, st);
-    __syncwarp();
-    if (iters != nullptr && lane == 0) iters[r] = it;
-    return;
-  }
-
-  // ---- fill pass and CBSR store
-  if (ok && eq && staged) {
+  if (exact_end && staged) {
     // the search ended on c(lo) == k: keep exactly {x >= lo}, in index order
     compact_ge<G, V>(x, lo, lane, stage);
   } else {
@@ -444,6 +395,68 @@ __device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>
     }
     __syncwarp();
   }
+}
+
+template <typename T, int G, bool EXACT, int L, typename IdxT>
+__device__ __forceinline__ void process_row_w1(const float (&x)[G][ElemTraits<T>::V], bool full, int64_t r,
+                                               int M, int k, int limit, bool cap_is_safety, float eps, int lane,
+                                               float2* __restrict__ stage, T* __restrict__ vals,
+                                               IdxT* __restrict__ idx, int* __restrict__ iters, uint32_t& st) {
+  constexpr int V = ElemTraits<T>::V;
+  constexpr int GS = 32 * V;
+  constexpr int NE = G * V;
+
+  // ---- value range (NaN-propagating; pads excluded from the minimum)
+  float mx = neg_inf(), mn = pos_inf();
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      mx = max_nan(mx, x[g][e]);
+      mn = min_nan(mn, (full || g * GS + lane * V + e < M) ? x[g][e] : pos_inf());
+    }
+  float hi = o2f(__reduce_max_sync(0xffffffffu, f2o(mx)));
+  float lo = o2f(__reduce_min_sync(0xffffffffu, f2o(mn)));
+  const bool ok = (lo >= -1e38f && hi <= 1e38f);
+  if (!ok) st |= (isfinite(lo) && isfinite(hi)) ? kStatusRange : kStatusNonFinite;
+
+  // ---- ties at the maximum: only possible if enough lanes hold the maximum
+  bool max_tie = false;
+  if (__popc(__ballot_sync(0xffffffffu, mx == hi)) * NE >= k) {
+    int c = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < V; ++e) c += (x[g][e] >= hi) ? 1 : 0;
+    max_tie = int(__reduce_add_sync(0xffffffffu, unsigned(c))) >= k;
+  }
+
+  int it = 0;
+  bool eq = false, comp = false;
+  int c_lo = M;
+  if (max_tie) {
+    lo = hi;           // keep the k lowest-index maxima through the fill rule:
+    hi = pos_inf();    // S is empty and every maximum is borderline
+  } else {
+    auto count_row = [&](float mid) { return __reduce_add_sync(0xffffffffu, lane_count_lt<G, V>(x, mid)); };
+    eq = search_passes<EXACT, L, decltype(count_row), (V == 8)>(count_row, 32 * NE, k, limit, cap_is_safety,
+                                                                 eps, lo, hi, it, c_lo, comp, st, iters == nullptr);
+  }
+  comp = comp && ok;
+
+  const int64_t obase = r * int64_t(k);
+  if (L > 0 && comp) {
+    // ---- compacted phase: list of the c(lo) <= 32 L elements >= lo
+    compact_ge<G, V>(x, lo, lane, stage);
+    __syncwarp();
+    finish_from_list<EXACT, (L > 0 ? L : 1), T, IdxT>(stage, c_lo, lo, hi, it, k, limit, cap_is_safety, eps,
+                                                     lane, vals, idx, obase, st);
+    __syncwarp();
+    if (iters != nullptr && lane == 0) iters[r] = it;
+    return;
+  }
+
+  fill_store_w1<T, G, IdxT>(x, lo, hi, ok && eq, k, lane, stage, vals, idx, obase);
   if (iters != nullptr && lane == 0) iters[r] = it;
 }
 

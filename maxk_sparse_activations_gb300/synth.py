@@ -19,7 +19,8 @@ import numpy as np
 
 __all__ = [
     "normal_f32", "uniform_pm1_f32", "int_ties_f32", "all_equal_rows_f32",
-    "outliers_f32", "subnormals_f32", "f32_to_bf16_bits", "normal_bf16",
+    "outliers_f32", "subnormals_f32", "wide_range_f32", "dense_bucket_f32", "negative_f32",
+    "signed_zeros_f32", "f32_to_bf16_bits", "normal_bf16",
     "make", "VALUE_SETS", "power_law_graph", "transpose_graph",
 ]
 
@@ -68,6 +69,37 @@ def subnormals_f32(N: int, M: int, seed: int = 0) -> np.ndarray:
     return (mant | sign).view(np.float32)
 
 
+def wide_range_f32(N: int, M: int, seed: int = 0) -> np.ndarray:
+    """Random sign times 10^U(-40, 37.5): magnitudes from binary32 subnormals to
+    3e37, across the range of every 16-bit format."""
+    g = _rng(seed)
+    mag = np.power(10.0, g.uniform(-40.0, 37.5, size=(N, M)))
+    sign = np.where(g.random((N, M)) < 0.5, -1.0, 1.0)
+    return (sign * mag).astype(np.float32)
+
+
+def dense_bucket_f32(N: int, M: int, seed: int = 0) -> np.ndarray:
+    """Every row a shuffle of 1 + j * 2^-23 for j = 0..M-1 (M <= 2^23): distinct
+    binary32 values, all within a few binary16 or bf16 spacings of 1."""
+    g = _rng(seed)
+    j = np.argsort(g.random((N, M)), axis=1).astype(np.float64)
+    return (1.0 + j * 2.0 ** -23).astype(np.float32)
+
+
+def negative_f32(N: int, M: int, seed: int = 0) -> np.ndarray:
+    """-|N(0, 1)|: every value negative."""
+    return -np.abs(_rng(seed).standard_normal((N, M), dtype=np.float32))
+
+
+def signed_zeros_f32(N: int, M: int, seed: int = 0) -> np.ndarray:
+    """Mostly -0.0 and +0.0 (fair sign), about one entry in eight N(0, 1)."""
+    g = _rng(seed)
+    x = np.where(g.random((N, M)) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+    hit = g.random((N, M)) < 0.125
+    x[hit] = g.standard_normal((N, M), dtype=np.float32)[hit]
+    return x
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bf16 (nearest, ties to even) and return the 16-bit patterns.
 
@@ -90,6 +122,10 @@ VALUE_SETS = {
     "all_equal": all_equal_rows_f32,
     "outliers": outliers_f32,
     "subnormal": subnormals_f32,
+    "wide_range": wide_range_f32,
+    "dense_bucket": dense_bucket_f32,
+    "negative": negative_f32,
+    "signed_zeros": signed_zeros_f32,
 }
 
 
