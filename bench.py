@@ -522,7 +522,19 @@ def _case_fused_backward():
         api.maxk_sspmm_backward_scatter(tp, tr, tw, dout, fi, M, grad=gx)
 
 
-PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward}
+def _case_maxk_forward():
+    # the MaxK forward of the fused-layer workload at a quarter of its rows:
+    # 2^18 x 256 bf16 N(0,1) -> CBSR k = 32 (bf16 values + int16 indices)
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    xb = torch.from_numpy(synth.normal_bf16(1 << 18, 256, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    for _ in range(3):
+        api.maxk_forward(xb, 32)
+
+
+PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward,
+                 "maxk-forward": _case_maxk_forward}
 
 
 def run_case(name: str) -> int:

@@ -50,6 +50,24 @@ struct Packed16;
 // fp32 rows: binary16 image
 template <>
 struct Packed16<float> {
+  static constexpr uint32_t kHalf2 = 0x38003800u;  // 0.5 in both halves
+  // (lo + hi) / 2 with one rounding: lo * 0.5 + (hi * 0.5); lies in [lo, hi]
+  static __device__ __forceinline__ uint32_t midpoint(uint32_t lo2, uint32_t hi2) {
+    uint32_t t, d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(hi2), "r"(kHalf2));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(lo2), "r"(kHalf2), "r"(t));
+    return d;
+  }
+  // lo < m < hi, on one half (both halves of each operand are equal)
+  static __device__ __forceinline__ bool strictly_inside(uint32_t lo2, uint32_t m2, uint32_t hi2) {
+    uint32_t r;
+    asm("{\n\t.reg .pred a, b, c, d;\n\t"
+        "setp.gt.f16x2 a|b, %1, %2;\n\t"
+        "setp.lt.and.f16x2 c|d, %1, %3, a;\n\t"
+        "selp.u32 %0, 1, 0, c;\n\t}"
+        : "=r"(r) : "r"(m2), "r"(lo2), "r"(hi2));
+    return r != 0u;
+  }
   static constexpr uint32_t kMagic2 = 0x64006400u;  // 1024.0 in both halves
   static constexpr uint32_t kFold = 0xc8006400u;     // (2 * 0x6400 << 16) + 0x6400
   static constexpr uint32_t kInf2 = 0x7c007c00u;     // +inf in both halves
@@ -90,6 +108,24 @@ struct Packed16<float> {
 // bf16 rows: the data themselves
 template <>
 struct Packed16<uint16_t> {
+  static constexpr uint32_t kHalf2 = 0x3f003f00u;  // 0.5 in both halves
+  // (lo + hi) / 2 with one rounding: lo * 0.5 + (hi * 0.5); lies in [lo, hi]
+  static __device__ __forceinline__ uint32_t midpoint(uint32_t lo2, uint32_t hi2) {
+    uint32_t t, d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(hi2), "r"(kHalf2));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(lo2), "r"(kHalf2), "r"(t));
+    return d;
+  }
+  // lo < m < hi, on one half (both halves of each operand are equal)
+  static __device__ __forceinline__ bool strictly_inside(uint32_t lo2, uint32_t m2, uint32_t hi2) {
+    uint32_t r;
+    asm("{\n\t.reg .pred a, b, c, d;\n\t"
+        "setp.gt.bf16x2 a|b, %1, %2;\n\t"
+        "setp.lt.and.bf16x2 c|d, %1, %3, a;\n\t"
+        "selp.u32 %0, 1, 0, c;\n\t}"
+        : "=r"(r) : "r"(m2), "r"(lo2), "r"(hi2));
+    return r != 0u;
+  }
   static constexpr uint32_t kMagic2 = 0x43004300u;  // 128.0 in both halves
   static constexpr uint32_t kFold = 0x86004300u;     // (2 * 0x4300 << 16) + 0x4300
   static constexpr uint32_t kInf2 = 0x7f807f80u;
@@ -139,12 +175,65 @@ __device__ __forceinline__ float next_up_bf16(float v) {
   return __uint_as_float((b & 0x80000000u) ? b - 0x10000u : b + 0x10000u);
 }
 
-// Writes the elements with h >= t2 (exactly `k` of them, an upper set of the
-// row) in ascending index order to stage[0 .. k).
+// Stages one kept element when `flag` is set: its value bits at word `pos` of
+// the warp's staging area and its index 256 words further on, then advances
+// pos. HALF selects the flag's half-word (0: bits 0..15, 1: bits 16..31).
+template <int HALF>
+__device__ __forceinline__ void stage_split_if(uint32_t flag, int& pos, uint32_t sbase, uint32_t v, int j) {
+  if (HALF == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .u32 a, t;\n\t"
+        "and.b32 t, %1, 65535;\n\t"
+        "setp.ne.u32 p, t, 0;\n\t"
+        "mad.lo.u32 a, %0, 4, %2;\n\t"
+        "@p st.shared.b32 [a], %3;\n\t"
+        "@p st.shared.b32 [a+1024], %4;\n\t"
+        "@p add.s32 %0, %0, 1;\n\t}"
+        : "+r"(pos) : "r"(flag), "r"(sbase), "r"(v), "r"(j) : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .u32 a;\n\t"
+        "setp.ge.u32 p, %1, 65536;\n\t"
+        "mad.lo.u32 a, %0, 4, %2;\n\t"
+        "@p st.shared.b32 [a], %3;\n\t"
+        "@p st.shared.b32 [a+1024], %4;\n\t"
+        "@p add.s32 %0, %0, 1;\n\t}"
+        : "+r"(pos) : "r"(flag), "r"(sbase), "r"(v), "r"(j) : "memory");
+  }
+}
+
+// Packed compares of one pass: s[w] = (h[w] >= t2) per half (1.0 or 0.0), and
+// cum[g] = magic + the 1.0s of groups 0..g, accumulated in the 16-bit format.
+template <typename P, int G, int WG>
+__device__ __forceinline__ void packed_pass(const uint32_t (&h)[G * WG], uint32_t t2, uint32_t (&s)[G * WG],
+                                            uint32_t (&cum)[G]) {
+  uint32_t acc = P::kMagic2;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int q = 0; q < WG; ++q) {
+      s[g * WG + q] = P::set_ge(h[g * WG + q], t2);
+      acc = P::add(acc, s[g * WG + q]);
+    }
+    cum[g] = acc;
+  }
+}
+
+// Lane count held in a packed accumulator (both halves, offsets removed).
+template <typename P>
+__device__ __forceinline__ uint32_t packed_lane_count(uint32_t acc) {
+  return (acc * 0x10001u - P::kFold) >> 16;
+}
+
+// Writes the elements of the pass whose compares are s[] / cum[] (exactly k of
+// them pass: an upper set of the row) in ascending index order: value bits to
+// words [0, k) of the staging area, indices to words [256, 256 + k). The
+// per-lane counts and the stored flags come from the same packed compares, so
+// the positions fill exactly [0, k).
 template <typename T, int G>
 __device__ __forceinline__ void compact_packed(const float (&x)[G][ElemTraits<T>::V],
-                                               const uint32_t (&h)[G * ElemTraits<T>::V / 2], uint32_t t2,
-                                               int k, int lane, float2* __restrict__ stage) {
+                                               const uint32_t (&s)[G * ElemTraits<T>::V / 2],
+                                               const uint32_t (&cum)[G], int lane, float2* __restrict__ stage) {
   using P = Packed16<T>;
   constexpr int V = ElemTraits<T>::V;
   constexpr int WG = V / 2;  // words per group
@@ -153,22 +242,18 @@ __device__ __forceinline__ void compact_packed(const float (&x)[G][ElemTraits<T>
   constexpr int FPW = 32 / FB;
   constexpr unsigned FMASK = (1u << FB) - 1u;
   constexpr int NWF = (G + FPW - 1) / FPW;
-  uint32_t s[G][WG];
   unsigned pkw[NWF];
 #pragma unroll
   for (int q = 0; q < NWF; ++q) pkw[q] = 0u;
+  unsigned prev = 0u;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    uint32_t acc = P::kMagic2;
-#pragma unroll
-    for (int q = 0; q < WG; ++q) {
-      s[g][q] = P::set_ge(h[g * WG + q], t2);
-      acc = P::add(acc, s[g][q]);
-    }
-    const unsigned c = (acc * 0x10001u - P::kFold) >> 16;
-    pkw[g / FPW] += c << (FB * (g % FPW));
+    const unsigned upto = packed_lane_count<P>(cum[g]);
+    pkw[g / FPW] += (upto - prev) << (FB * (g % FPW));
+    prev = upto;
   }
   const int jl = lane * V;
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
   int base = 0;
 #pragma unroll
   for (int q = 0; q < NWF; ++q) {
@@ -181,16 +266,8 @@ __device__ __forceinline__ void compact_packed(const float (&x)[G][ElemTraits<T>
         int pos = base + int((ex >> (FB * f)) & FMASK);
 #pragma unroll
         for (int w = 0; w < WG; ++w) {
-          // (pos < k holds whenever exactly k elements pass; the test keeps every
-          // store inside the staging row regardless)
-          if ((s[g][w] & 0xffffu) && pos < k) {
-            stage[pos] = make_float2(x[g][2 * w], __int_as_float(g * GS + jl + 2 * w));
-            ++pos;
-          }
-          if ((s[g][w] >> 16) && pos < k) {
-            stage[pos] = make_float2(x[g][2 * w + 1], __int_as_float(g * GS + jl + 2 * w + 1));
-            ++pos;
-          }
+          stage_split_if<0>(s[g * WG + w], pos, sbase, __float_as_uint(x[g][2 * w]), g * GS + jl + 2 * w);
+          stage_split_if<1>(s[g * WG + w], pos, sbase, __float_as_uint(x[g][2 * w + 1]), g * GS + jl + 2 * w + 1);
         }
         base += int((tot >> (FB * f)) & FMASK);
       }
@@ -238,37 +315,40 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
   // or, for k <= 32, of the smallest lane maximum (each of the 32 lanes holds an
   // element at least that large, so C(lo) >= 32 >= k)
   const uint32_t hi2 = P::splat(hi32);
-  float hi = P::low_f32(hi2);
+  const float hi_img = P::low_f32(hi2);
   const float lo_src = (k <= 32) ? o2f(__reduce_min_sync(FULL, f2o(mx))) : lo32;
-  float lo = P::low_f32(P::splat(lo_src));
 
   float b_lo, b_hi;  // coarse bucket [b_lo, b_hi) that the binary32 search finishes
   // ties at the top image: only possible when enough lanes' maxima share it
-  if (__popc(__ballot_sync(FULL, P::low_f32(P::splat(mx)) >= hi)) * NE >= k && count(hi2) >= k) {
-    b_lo = hi;
+  if (__popc(__ballot_sync(FULL, P::low_f32(P::splat(mx)) >= hi_img)) * NE >= k && count(hi2) >= k) {
+    b_lo = hi_img;
     b_hi = pos_inf();
   } else {
+    // coarse bisection on the packed bracket (both halves of lo2 / hi2 equal)
     bool eq = false;
-    uint32_t t2 = 0u;
+    uint32_t lo2 = P::splat(lo_src), hi2_ = hi2;
+    const uint32_t k0 = uint32_t(k) << 16, k1 = uint32_t(k + 1) << 16;  // C(t) >= k, >= k + 1 on the redux word
+    uint32_t sp[NW], cum[G];  // the last pass's compares, kept for the fill
     for (;;) {
-      const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
-      t2 = P::splat(mid);
-      const float m = P::low_f32(t2);
-      if (!(lo < m && m < hi)) break;  // no 16-bit value strictly inside
-      const int cnt = count(t2);
-      if (cnt == k) { eq = true; break; }
-      const bool ge = cnt > k;
-      lo = ge ? m : lo;
-      hi = ge ? hi : m;
+      const uint32_t m2 = P::midpoint(lo2, hi2_);
+      if (!P::strictly_inside(lo2, m2, hi2_)) break;  // no 16-bit value strictly inside
+      packed_pass<P, G, V / 2>(h, m2, sp, cum);
+      const uint32_t tot = __reduce_add_sync(FULL, cum[G - 1] * 0x10001u - P::kFold);
+      const bool ge = tot >= k0;
+      if (ge && tot < k1) { eq = true; break; }
+      lo2 = ge ? m2 : lo2;
+      hi2_ = ge ? hi2_ : m2;
     }
+    const float lo = P::low_f32(lo2), hi = P::low_f32(hi2_);
     const int64_t obase = r * int64_t(k);
     if (eq) {
-      compact_packed<T, G>(x, h, t2, k, lane, stage);
+      compact_packed<T, G>(x, sp, cum, lane, stage);
       __syncwarp();
+      const float* sv = reinterpret_cast<const float*>(stage);
+      const int* si = reinterpret_cast<const int*>(stage) + kStageK;
       for (int p = lane; p < k; p += 32) {
-        const float2 e = stage[p];
-        vals[obase + p] = out_value(e.x, vals);
-        idx[obase + p] = IdxT(__float_as_int(e.y));
+        vals[obase + p] = out_value(sv[p], vals);
+        idx[obase + p] = IdxT(si[p]);
       }
       __syncwarp();
       return;
@@ -305,15 +385,36 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
   fill_store_w1<T, G, IdxT>(x, flo, fhi, eq32, k, lane, stage, vals, idx, r * int64_t(k));
 }
 
-// Minimum resident blocks per SM of the packed kernel.
-template <int NE>
+// fp32 rows (1 KB at M = 256) load the warp's next row into registers while
+// the current one is searched; bf16 rows (half the bytes) measured faster
+// without it (GB300, 2^20 x 256, k = 32, 4 blocks per SM: fp32 445 vs 469 us,
+// bf16 519 vs 487 us).
+#ifndef RTOPK_PACKED_PREFETCH_F32
+#define RTOPK_PACKED_PREFETCH_F32 1
+#endif
+template <typename T>
+struct PackedPrefetch {
+  static constexpr bool value = sizeof(T) == 4 && RTOPK_PACKED_PREFETCH_F32;
+};
+
+// Minimum resident blocks per SM of the packed kernel. With the prefetch, 4
+// blocks of 256 (64 registers) measured faster than 5 (48 registers, a small
+// spill): 435.5 against 440.3 us at 2^20 x 256 fp32, k = 32.
+#ifndef RTOPK_PACKED_MIN_BLOCKS
+#define RTOPK_PACKED_MIN_BLOCKS 5
+#endif
+#ifndef RTOPK_PACKED_PREFETCH_MIN_BLOCKS
+#define RTOPK_PACKED_PREFETCH_MIN_BLOCKS 4
+#endif
+template <typename T, int NE>
 struct PackedOcc {
-  static constexpr int value = NE <= 8 ? 5 : 3;
+  static constexpr int value =
+      NE <= 8 ? (PackedPrefetch<T>::value ? RTOPK_PACKED_PREFETCH_MIN_BLOCKS : RTOPK_PACKED_MIN_BLOCKS) : 3;
 };
 
 // Rows of exactly G * 32 * V elements, 16-byte aligned, exact mode, k <= kStageK.
 template <typename T, int G, typename IdxT>
-__global__ void __launch_bounds__(256, PackedOcc<G * ElemTraits<T>::V>::value)
+__global__ void __launch_bounds__(256, PackedOcc<T, G * ElemTraits<T>::V>::value)
 rtopk_warp_packed_kernel(const T* __restrict__ in, int64_t N, int M, int k, T* __restrict__ vals,
                          IdxT* __restrict__ idx, uint32_t* __restrict__ status) {
   constexpr int V = ElemTraits<T>::V;
@@ -323,10 +424,25 @@ rtopk_warp_packed_kernel(const T* __restrict__ in, int64_t N, int M, int k, T* _
   float2* stage = stage_all[wib];
   const int64_t nwarps = int64_t(gridDim.x) * 8;
   uint32_t st = 0;
-  for (int64_t r = int64_t(blockIdx.x) * 8 + wib; r < N; r += nwarps) {
-    float x[G][V];
-    load_row<G, 1, true>(in + r * int64_t(M), M, 0, lane, true, x);
-    process_row_packed<T, G, IdxT>(x, r, M, k, lane, stage, vals, idx, st);
+  if constexpr (PackedPrefetch<T>::value) {
+    float xn[G][V];
+    int64_t r = int64_t(blockIdx.x) * 8 + wib;
+    if (r < N) load_row<G, 1, true>(in + r * int64_t(M), M, 0, lane, true, xn);
+    for (; r < N; r += nwarps) {
+      float x[G][V];
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < V; ++e) x[g][e] = xn[g][e];
+      if (r + nwarps < N) load_row<G, 1, true>(in + (r + nwarps) * int64_t(M), M, 0, lane, true, xn);
+      process_row_packed<T, G, IdxT>(x, r, M, k, lane, stage, vals, idx, st);
+    }
+  } else {
+    for (int64_t r = int64_t(blockIdx.x) * 8 + wib; r < N; r += nwarps) {
+      float x[G][V];
+      load_row<G, 1, true>(in + r * int64_t(M), M, 0, lane, true, x);
+      process_row_packed<T, G, IdxT>(x, r, M, k, lane, stage, vals, idx, st);
+    }
   }
   if (status != nullptr && st != 0u && lane == 0) atomicOr(status, st);
 }
