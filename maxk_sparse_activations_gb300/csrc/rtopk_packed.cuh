@@ -285,18 +285,36 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
   constexpr int NW = NE / 2;
   constexpr unsigned FULL = 0xffffffffu;
 
-  // ---- value range (binary32, NaN-propagating) and the precondition
-  float mx = neg_inf(), mn = pos_inf();
+  // ---- value range (binary32, NaN-propagating) and the precondition. For
+  // k <= 32 the search starts from the smallest lane maximum, so the row
+  // minimum is not needed: the precondition is checked on max |x| instead.
+  float mx = neg_inf();
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-      mx = max_nan(mx, x[g][e]);
-      mn = min_nan(mn, x[g][e]);
-    }
+    for (int e = 0; e < V; ++e) mx = max_nan(mx, x[g][e]);
   const float hi32 = o2f(__reduce_max_sync(FULL, f2o(mx)));
-  const float lo32 = o2f(__reduce_min_sync(FULL, f2o(mn)));
-  if (!(lo32 >= -1e38f && hi32 <= 1e38f)) {
+  float lo_src;
+  bool valid;
+  if (k <= 32) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(x[g][e]));
+    valid = __all_sync(FULL, amax <= 1e38f);
+    // each of the 32 lanes holds an element >= its maximum: C(lane-max minimum) >= 32 >= k
+    lo_src = o2f(__reduce_min_sync(FULL, f2o(mx)));
+  } else {
+    float mn = pos_inf();
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < V; ++e) mn = min_nan(mn, x[g][e]);
+    lo_src = o2f(__reduce_min_sync(FULL, f2o(mn)));
+    valid = lo_src >= -1e38f && hi32 <= 1e38f;
+  }
+  if (!valid) {
     // invalid row: the binary32 path flags it and keeps every write in the row
     process_row_w1<T, G, true, 0, IdxT>(x, true, r, M, k, kSafetyCap, true, 0.0f, lane, stage, vals, idx,
                                         nullptr, st);
@@ -311,12 +329,10 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
     for (int w = 0; w < V / 2; ++w) h[g * (V / 2) + w] = P::pack(x[g][2 * w + 1], x[g][2 * w]);
   auto count = [&](uint32_t t2) { return int(__reduce_add_sync(FULL, packed_count_hi16<P, NW>(h, 0, NW, t2)) >> 16); };
 
-  // ---- coarse bracket: hi = image of the maximum; lo = image of the minimum,
-  // or, for k <= 32, of the smallest lane maximum (each of the 32 lanes holds an
-  // element at least that large, so C(lo) >= 32 >= k)
+  // ---- coarse bracket: hi = image of the maximum; lo = image of lo_src (the
+  // minimum, or for k <= 32 the smallest lane maximum)
   const uint32_t hi2 = P::splat(hi32);
   const float hi_img = P::low_f32(hi2);
-  const float lo_src = (k <= 32) ? o2f(__reduce_min_sync(FULL, f2o(mx))) : lo32;
 
   float b_lo, b_hi;  // coarse bucket [b_lo, b_hi) that the binary32 search finishes
   // ties at the top image: only possible when enough lanes' maxima share it
@@ -329,12 +345,23 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
     uint32_t lo2 = P::splat(lo_src), hi2_ = hi2;
     const uint32_t k0 = uint32_t(k) << 16, k1 = uint32_t(k + 1) << 16;  // C(t) >= k, >= k + 1 on the redux word
     uint32_t sp[NW], cum[G];  // the last pass's compares, kept for the fill
+    // Two passes per iteration; only the first tests for collapse. The midpoint
+    // always lies in [lo, hi], so once no 16-bit value is strictly inside, the
+    // second pass counts at lo (C > k: lo unchanged) or at hi (C < k: hi
+    // unchanged) and the next iteration's test ends the search.
     for (;;) {
-      const uint32_t m2 = P::midpoint(lo2, hi2_);
+      uint32_t m2 = P::midpoint(lo2, hi2_);
       if (!P::strictly_inside(lo2, m2, hi2_)) break;  // no 16-bit value strictly inside
       packed_pass<P, G, V / 2>(h, m2, sp, cum);
-      const uint32_t tot = __reduce_add_sync(FULL, cum[G - 1] * 0x10001u - P::kFold);
-      const bool ge = tot >= k0;
+      uint32_t tot = __reduce_add_sync(FULL, cum[G - 1] * 0x10001u - P::kFold);
+      bool ge = tot >= k0;
+      if (ge && tot < k1) { eq = true; break; }
+      lo2 = ge ? m2 : lo2;
+      hi2_ = ge ? hi2_ : m2;
+      m2 = P::midpoint(lo2, hi2_);
+      packed_pass<P, G, V / 2>(h, m2, sp, cum);
+      tot = __reduce_add_sync(FULL, cum[G - 1] * 0x10001u - P::kFold);
+      ge = tot >= k0;
       if (ge && tot < k1) { eq = true; break; }
       lo2 = ge ? m2 : lo2;
       hi2_ = ge ? hi2_ : m2;
