@@ -341,34 +341,11 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
     b_hi = pos_inf();
   } else {
     // coarse bisection on the packed bracket (both halves of lo2 / hi2 equal)
-    bool eq = false;
     uint32_t lo2 = P::splat(lo_src), hi2_ = hi2;
     const uint32_t k0 = uint32_t(k) << 16, k1 = uint32_t(k + 1) << 16;  // C(t) >= k, >= k + 1 on the redux word
-    uint32_t sp[NW], cum[G];  // the last pass's compares, kept for the fill
-    // Two passes per iteration; only the first tests for collapse. The midpoint
-    // always lies in [lo, hi], so once no 16-bit value is strictly inside, the
-    // second pass counts at lo (C > k: lo unchanged) or at hi (C < k: hi
-    // unchanged) and the next iteration's test ends the search.
-    for (;;) {
-      uint32_t m2 = P::midpoint(lo2, hi2_);
-      if (!P::strictly_inside(lo2, m2, hi2_)) break;  // no 16-bit value strictly inside
-      packed_pass<P, G, V / 2>(h, m2, sp, cum);
-      uint32_t tot = __reduce_add_sync(FULL, cum[G - 1] * 0x10001u - P::kFold);
-      bool ge = tot >= k0;
-      if (ge && tot < k1) { eq = true; break; }
-      lo2 = ge ? m2 : lo2;
-      hi2_ = ge ? hi2_ : m2;
-      m2 = P::midpoint(lo2, hi2_);
-      packed_pass<P, G, V / 2>(h, m2, sp, cum);
-      tot = __reduce_add_sync(FULL, cum[G - 1] * 0x10001u - P::kFold);
-      ge = tot >= k0;
-      if (ge && tot < k1) { eq = true; break; }
-      lo2 = ge ? m2 : lo2;
-      hi2_ = ge ? hi2_ : m2;
-    }
-    const float lo = P::low_f32(lo2), hi = P::low_f32(hi2_);
     const int64_t obase = r * int64_t(k);
-    if (eq) {
+    // C(t) == k: {h >= t} is the row's top-k; written from the pass's compares
+    auto finish = [&](const uint32_t (&sp)[NW], const uint32_t (&cum)[G]) {
       compact_packed<T, G>(x, sp, cum, lane, stage);
       __syncwarp();
       const float* sv = reinterpret_cast<const float*>(stage);
@@ -378,8 +355,32 @@ __device__ __forceinline__ void process_row_packed(const float (&x)[G][ElemTrait
         idx[obase + p] = IdxT(si[p]);
       }
       __syncwarp();
-      return;
+    };
+    // Two passes per iteration; only the first tests for collapse. The midpoint
+    // always lies in [lo, hi], so once no 16-bit value is strictly inside, the
+    // second pass counts at lo (C > k: lo unchanged) or at hi (C < k: hi
+    // unchanged) and the next iteration's test ends the search. Each pass
+    // keeps its own compares and writes the row from them where it ends.
+    for (;;) {
+      uint32_t m2 = P::midpoint(lo2, hi2_);
+      if (!P::strictly_inside(lo2, m2, hi2_)) break;  // no 16-bit value strictly inside
+      uint32_t sa[NW], ca[G];
+      packed_pass<P, G, V / 2>(h, m2, sa, ca);
+      uint32_t tot = __reduce_add_sync(FULL, ca[G - 1] * 0x10001u - P::kFold);
+      bool ge = tot >= k0;
+      if (ge && tot < k1) { finish(sa, ca); return; }
+      lo2 = ge ? m2 : lo2;
+      hi2_ = ge ? hi2_ : m2;
+      m2 = P::midpoint(lo2, hi2_);
+      uint32_t sb[NW], cb[G];
+      packed_pass<P, G, V / 2>(h, m2, sb, cb);
+      tot = __reduce_add_sync(FULL, cb[G - 1] * 0x10001u - P::kFold);
+      ge = tot >= k0;
+      if (ge && tot < k1) { finish(sb, cb); return; }
+      lo2 = ge ? m2 : lo2;
+      hi2_ = ge ? hi2_ : m2;
     }
+    const float lo = P::low_f32(lo2), hi = P::low_f32(hi2_);
     if (sizeof(T) == 2 && next_up_bf16(lo) == hi) {
       // bf16 rows: B = {x == lo}, all tied; keep x >= hi and fill from B by index
       fill_store_w1<T, G, IdxT>(x, lo, hi, false, k, lane, stage, vals, idx, obase);
