@@ -117,6 +117,11 @@ int rtopk_select(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_it
  *
  *  iters   device, N int32 or NULL: counted bisection passes of each row
  *  status  device, one uint32 or NULL: OR of RTOPK_STATUS_* bits over all rows
+ * Performance note: with iters != NULL every row runs the binary32 search whose
+ * passes are counted. In exact mode with iters == NULL (and in rtopk_select /
+ * maxk_forward) rows of 128..512 elements may instead run a search counted on
+ * packed 16-bit images of the row, finished in binary32 where needed: same
+ * outputs, fewer instructions.
  */
 int rtopk_select_stats(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_iter,
                        float eps, int32_t dtype, void* vals, int32_t* idx, int32_t* iters,
