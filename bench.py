@@ -41,6 +41,32 @@ WORKLOAD = ("rtopk_select exact (max_iter=-1, eps=0), N=2^20 rows x M=256 fp32 i
 PROFILE_GLOB = os.path.join(ROOT, "profiles", "*.md")
 
 
+def workload_config(world: int) -> dict:
+    """The `config` object of both arms' JSON lines (the same workload on each)."""
+    return {"workload": WORKLOAD, "N": N_ROWS, "M": M_COLS, "k": K_SEL, "max_iter": -1, "eps": 0.0,
+            "l2": f"inputs larger than L2 ({N_ROWS * M_COLS * 4 / 1e9:.2f} GB per rank; L2 129 MB)",
+            "parallelism": f"rows: one {N_ROWS}-row batch per rank x {world}"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model string (/proc/cpuinfo; Arm hosts report no model name)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                val = line.split(":", 1)[1].strip()
+                if key == "CPU part":
+                    parts = {"0xd4f": "Neoverse-V2 (Grace)", "0xd40": "Neoverse-V1", "0xd8e": "Neoverse-N3"}
+                    return f"Arm {parts.get(val, 'CPU part ' + val)}"
+                return val
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def algorithmic_bytes(N, M, k, s_in, s_val, s_idx):
     """Bytes the method must move: read the matrix once, write the CBSR arrays once."""
     return N * M * s_in + N * k * (s_val + s_idx)
@@ -90,7 +116,72 @@ def measured_peaks():
 # ------------------------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ------------------------------------------------------------------------------------------
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons polled through NVML (the driver's
+    libnvidia-ml, loaded with ctypes) every ~2 ms on a thread: short timed
+    regions (tens of ms) still get samples. Only reads; changes no setting."""
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_uuid: str | None):
+        import ctypes
+        self.ct = ctypes
+        if not gpu_uuid:  # NVML numbers GPUs independently of CUDA_VISIBLE_DEVICES: go by UUID only
+            raise OSError("no GPU UUID")
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(gpu_uuid.encode()), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + gpu_uuid)
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        self.samples: list[tuple[float, float, float, int]] = []
+        self._stop = threading.Event()
+        self.thread = None
+
+    def _one(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        self.lib.nvmlDeviceGetClockInfo(self.h, ct.c_int(1), ct.byref(mhz))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reason_fn(self.h, ct.byref(rs))
+        return float(mhz.value), mw.value / 1000.0, int(rs.value)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            t = time.time()
+            mhz, w, rs = self._one()
+            self.samples.append((t, mhz, w, rs))
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+        time.sleep(0.02)
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no NVML samples"], "samples": 0,
+                    "source": "nvml"}
+        reasons = sorted({name for s in inside for bit, name in self.REASONS.items() if s[3] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(s[2] for s in inside),
+                "source": "nvml, ~2 ms polling"}
+
+
 class ClockSampler:
+    """nvidia-smi at 50 ms intervals: the fallback when NVML cannot be loaded."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -147,11 +238,18 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
                 "reasons": reasons, "samples": len(inside),
                 "power_w_max": max((float(r[3]) for r in used if r[3].replace(".", "", 1).isdigit()),
-                                   default=None)}
+                                   default=None), "source": "nvidia-smi, 50 ms"}
+
+
+def make_clock_sampler(uuid: str | None):
+    try:
+        return NvmlClockSampler(uuid)
+    except (OSError, AttributeError):
+        return ClockSampler(uuid)
 
 
 def rejected_clocks(c: dict) -> bool:
-    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "hw_power_brake_slowdown"}
     if bad & set(c.get("reasons", [])):
         return True
     if c.get("sm_mhz") and c.get("sm_max_mhz") and c["sm_mhz"] < 0.6 * c["sm_max_mhz"] \
@@ -163,8 +261,9 @@ def rejected_clocks(c: dict) -> bool:
 # ------------------------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline field)
 # ------------------------------------------------------------------------------------------
-def time_oracle(x: np.ndarray, k: int, threads: int, min_seconds: float, max_reps: int):
-    """Wall time of the oracle replay over x split into `threads` contiguous row blocks."""
+def time_oracle(x: np.ndarray, k: int, threads: int, min_seconds: float, max_reps: int, fn: str = "replay"):
+    """Wall time of the oracle replay (or, fn="sort_topk", the sort definition)
+    over x split into `threads` contiguous row blocks."""
     import concurrent.futures as cf
     import oracle  # test infrastructure; only the CPU-baseline leg uses it
     oracle.build()
@@ -172,7 +271,10 @@ def time_oracle(x: np.ndarray, k: int, threads: int, min_seconds: float, max_rep
 
     def work(rows):
         if rows.size:
-            oracle.replay(x[rows[0]:rows[-1] + 1], k, -1, 0.0)
+            if fn == "replay":
+                oracle.replay(x[rows[0]:rows[-1] + 1], k, -1, 0.0)
+            else:
+                oracle.sort_topk(x[rows[0]:rows[-1] + 1], k)
 
     best, reps, t_all = None, 0, time.perf_counter()
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
@@ -194,7 +296,7 @@ def run_reference(args, rank: int, world: int):
     probe = synth.normal_f32(16384, M_COLS, seed=0)
     t_probe, _ = time_oracle(probe, K_SEL, threads, 0.0, 1)
     rate = probe.shape[0] / max(t_probe, 1e-9)
-    budget = 60.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     rows = int(min(N_ROWS, max(4096, rate * budget)))
     x = synth.normal_f32(N_ROWS, M_COLS, seed=0)[:rows]
     for _ in range(args.warmup):
@@ -209,9 +311,9 @@ def run_reference(args, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "N": N_ROWS, "M": M_COLS, "k": K_SEL, "sample_rows": rows},
+        "config": workload_config(world),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "sample_rows": rows, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -276,7 +378,7 @@ def run_gb300(args, rank: int, world: int):
         pass
     clocks = None
     for attempt in range(2):
-        sampler = ClockSampler(uuid) if rank == 0 else None
+        sampler = make_clock_sampler(uuid) if rank == 0 else None
         if sampler:
             sampler.start()
         w0 = time.time()
@@ -323,17 +425,26 @@ def run_gb300(args, rank: int, world: int):
         if not args.no_cpu_baseline:
             threads = os.cpu_count() or 1
             t_cpu, reps = time_oracle(x_host, K_SEL, threads, 5.0, 3)
+            # single-threaded replay and sort definition on bounded row samples
+            n1, ns = min(N_ROWS, 1 << 16), min(N_ROWS, 1 << 14)
+            t_one, _ = time_oracle(x_host[:n1], K_SEL, 1, 0.0, 1)
+            t_sort, _ = time_oracle(x_host[:ns], K_SEL, 1, 0.0, 1, fn="sort_topk")
+            t_sort_all, _ = time_oracle(x_host[:n1], K_SEL, threads, 0.0, 1, fn="sort_topk")
             cpu = {"value": N_ROWS / t_cpu, "unit": "rows/s", "cores": threads, "kind": "oracle",
-                   "sample": f"all 2^20 rows of the workload, oracle replay (exact), best of {reps}, "
-                             f"{threads} threads on contiguous row blocks"}
+                   "sample": f"all {N_ROWS} rows of the workload, oracle replay (exact), best of {reps}, "
+                             f"{threads} threads on contiguous row blocks",
+                   "cpu_model": cpu_model(),
+                   "replay_single_thread_rows_per_s": n1 / t_one,
+                   "replay_single_thread_sample": f"first {n1} rows, 1 thread",
+                   "sort_topk_single_thread_rows_per_s": ns / t_sort,
+                   "sort_topk_single_thread_sample": f"first {ns} rows, 1 thread",
+                   "sort_topk_all_cores_rows_per_s": n1 / t_sort_all}
         line = {
             "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "N": N_ROWS, "M": M_COLS, "k": K_SEL, "max_iter": -1,
-                       "eps": 0.0, "l2": "inputs larger than L2 (1.07 GB per rank; L2 129 MB)",
-                       "parallelism": f"rows: one 2^20-row batch per rank x {world}"},
+            "config": workload_config(world),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
@@ -477,6 +588,74 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
                                           "unfused_chain_us": t_ch * 1e3}
     del agg, gx, dsp, dsp16, g
 
+    # configuration 3 (shape sweep) and configuration 4 (long rows, adversarial
+    # values): throughput tables, each launch timed alone with L2 flushed before it
+    peak, _ = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed_cold(fn, reps):
+        ms = []
+        for _ in range(reps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    sweep = {}
+    n3 = 1 << 18
+    gen = torch.Generator(device=dev).manual_seed(0)
+    for m3 in (128, 256, 512, 1024):
+        x32 = torch.randn(n3, m3, device=dev, generator=gen)
+        for dt, xx in (("f32", x32), ("bf16", x32.to(torch.bfloat16))):
+            s_in = xx.element_size()
+            for k3 in (16, 32, 64, 128, 256):
+                if k3 >= m3:
+                    continue
+                v3 = torch.empty((n3, k3), dtype=xx.dtype, device=dev)
+                i3 = torch.empty((n3, k3), dtype=torch.int32, device=dev)
+                for mi in (-1, 2):
+                    f = lambda: api.rtopk_select(xx, k3, mi, vals=v3, idx=i3)
+                    f()
+                    t = timed_cold(f, 7)
+                    by = algorithmic_bytes(n3, m3, k3, s_in, s_in, 4)
+                    sweep[f"{dt}_M{m3}_k{k3}_{'exact' if mi < 0 else 'max_iter_2'}"] = {
+                        "us": t * 1e3, "gbs": by / (t * 1e-3) / 1e9, "frac_of_measured_hbm": by / (t * 1e-3) / 1e9 / peak,
+                        "rows_per_s": n3 / (t * 1e-3)}
+                del v3, i3
+        del x32, xx
+    out["config3_sweep_N2^18"] = sweep
+    long_rows = {}
+    n4 = 65536
+    for m4 in (2048, 4096, 8192):
+        x4 = torch.rand(n4, m4, device=dev, generator=gen) * 2 - 1
+        sets = {"uniform": x4}
+        xo = torch.randn(n4, m4, device=dev, generator=gen)
+        hit = torch.rand(n4, m4, device=dev, generator=gen) < 0.01
+        sign = torch.where(torch.rand(n4, m4, device=dev, generator=gen) < 0.5, -1e30, 1e30)
+        sets["outliers_1e30"] = torch.where(hit, sign, xo)
+        del xo, hit, sign
+        for name, xx in sets.items():
+            for k4 in (64, 256, 1024):
+                v4 = torch.empty((n4, k4), dtype=torch.float32, device=dev)
+                i4 = torch.empty((n4, k4), dtype=torch.int32, device=dev)
+                f = lambda: api.rtopk_select(xx, k4, vals=v4, idx=i4)
+                f()
+                t = timed_cold(f, 5)
+                by = algorithmic_bytes(n4, m4, k4, 4, 4, 4)
+                long_rows[f"{name}_M{m4}_k{k4}"] = {
+                    "us": t * 1e3, "gbs": by / (t * 1e-3) / 1e9, "frac_of_measured_hbm": by / (t * 1e-3) / 1e9 / peak,
+                    "rows_per_s": n4 / (t * 1e-3)}
+                del v4, i4
+        del sets, x4
+    out["config4_long_rows_N65536"] = long_rows
+    del flush
+    torch.cuda.empty_cache()
+
     # rows past the pages' 8192-element limit: one CTA cluster per row
     for Ml, Nl, kl in ((16384, 16384, 256), (65536, 4096, 256)):
         xl = torch.randn(Nl, Ml, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
@@ -558,12 +737,27 @@ def main():
     ap.add_argument("--case", choices=sorted(PROFILE_CASES),
                     help="run three launches of one secondary kernel on its workload and exit "
                          "(a small, self-contained target for profiler captures; prints no JSON)")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: CPU seconds the whole run's sampled steps aim for")
     args = ap.parse_args()
     N_ROWS = args.rows
     if args.case:
         return run_case(args.case)
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # N ranks, one process per GPU, launched the way torchrun launches them
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        return subprocess.call(cmd)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU")
     if world > 1:
         import torch
         import torch.distributed as dist

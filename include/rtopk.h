@@ -112,8 +112,8 @@ int rtopk_select(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_it
 
 /*
  * rtopk_select_stats -- rtopk_select plus diagnostics (same kernel, same outputs).
- * [RTopK] "Surprising findings" (exact selection exits within 16 iterations in
- * most cases) -- `iters` measures exactly that per row.
+ * [RTopK] "Surprising findings" (the exact search usually ends after a small,
+ * bounded number of passes) -- `iters` gives that pass count for every row.
  *
  *  iters   device, N int32 or NULL: counted bisection passes of each row
  *  status  device, one uint32 or NULL: OR of RTOPK_STATUS_* bits over all rows

@@ -34,3 +34,24 @@ def assert_same_selection(gv, gi, ov, oi, rows=None, what=""):
     bad = np.flatnonzero((gi != oi).any(axis=1) | (gv != ref_bits(ov)).any(axis=1))
     assert bad.size == 0, (f"{what}: {bad.size} rows differ; first row {bad[0]}: "
                            f"gpu idx {gi[bad[0]][:16]} oracle idx {oi[bad[0]][:16]}")
+
+
+def oracle_rows(fn, x, *args, threads=None):
+    """Run an oracle function over contiguous row blocks of x on every host
+    core and stack the per-block results (the oracle's C code releases the GIL
+    inside ctypes calls, so the blocks run in parallel). Results are the same
+    as one call over all rows: every oracle function works row by row."""
+    import concurrent.futures as cf
+    import os
+
+    n = x.shape[0]
+    threads = threads or min(32, os.cpu_count() or 1)
+    if n < 4096 or threads == 1:
+        return fn(x, *args)
+    bounds = np.linspace(0, n, threads + 1).astype(np.int64)
+    blocks = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    with cf.ThreadPoolExecutor(max_workers=len(blocks)) as ex:
+        parts = list(ex.map(lambda ab: fn(x[ab[0]:ab[1]], *args), blocks))
+    if isinstance(parts[0], tuple):
+        return tuple(np.concatenate([p[j] for p in parts]) for j in range(len(parts[0])))
+    return np.concatenate(parts)

@@ -28,8 +28,8 @@ def test_profiled_traffic_needs_the_matching_source_hash():
 
 
 def test_reference_arm_prints_one_json_line():
-    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
-                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+                        "--ref-seconds", "4"], cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-2000:]
     line = json.loads(p.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference"
@@ -38,3 +38,6 @@ def test_reference_arm_prints_one_json_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+    # the same workload keys as the GPU arm's line
+    assert line["config"] == bench.workload_config(1)
+    assert line["cpu_baseline"]["cpu_model"]

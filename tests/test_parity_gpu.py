@@ -13,7 +13,7 @@ import torch
 import oracle
 from maxk_sparse_activations_gb300 import accuracy, api, synth
 
-from gpu_util import assert_same_selection, to_dev, vals_np
+from gpu_util import assert_same_selection, oracle_rows, to_dev, vals_np
 
 pytestmark = pytest.mark.gpu
 
@@ -82,35 +82,52 @@ def test_config3_sweep_reduced(M, dtype):
 
 @pytest.mark.parametrize("N", [1 << 16, 1 << 18, 1 << 20])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_config3_full_rows_sampled(N, dtype):
+def test_config3_full_rows(N, dtype):
+    """The sweep's full batch sizes at M = 256, k = 32, compared on every row:
+    exact with pass counts, the default call (no pass counts: the packed
+    search), max_iter = 2 and eps = 1e-2."""
     M, k = 256, 32
     x = synth.make("normal", N, M, seed=0, dtype=dtype)
-    rows = _sample_rows(N, 3000)
+    xt = to_dev(x)
     for m, eps in ((-1, 0.0), (2, 0.0), (-1, 1e-2)):
-        v, i, it, st = _run(x, k, m, eps)
-        assert st == 0
-        ov, oi, oit = oracle.replay(x[rows], k, m, eps)
-        assert_same_selection(v, i, ov, oi, rows=rows, what=f"N={N} {dtype} max_iter={m} eps={eps}")
-        np.testing.assert_array_equal(it[rows], oit)
+        v, i, it, st = api.rtopk_select_stats(xt, k, m, eps)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ov, oi, oit = oracle_rows(oracle.replay, x, k, m, eps)
+        assert_same_selection(v, i, ov, oi, what=f"N={N} {dtype} max_iter={m} eps={eps}")
+        np.testing.assert_array_equal(it.cpu().numpy(), oit)
+        if m < 0 and eps == 0.0:
+            v, i = api.rtopk_select(xt, k)
+            torch.cuda.synchronize()
+            assert_same_selection(v, i, ov, oi, what=f"N={N} {dtype} default path")
 
 
 # ---- configuration 4: long rows, adversarial values ------------------------------------
 @pytest.mark.parametrize("value_set", ["uniform", "int_ties", "all_equal", "outliers", "subnormal"])
 @pytest.mark.parametrize("M", [2048, 4096, 8192])
 def test_config4_long_rows_adversarial(M, value_set):
+    """Every one of the 65,536 rows, k in {64, 256, 1024}, through both calls:
+    rtopk_select_stats (binary32 search from [min, max], pass counts compared)
+    and rtopk_select (no pass counts: the block kernel's raised lower end and
+    its shared-list tail), each against the oracle's exact replay, which the
+    pins tie to the definition."""
     N = 65536
     x = synth.make(value_set, N, M, seed=0)
-    rows = _sample_rows(N, 300)
     xt = to_dev(x)
     for k in (64, 256, 1024):
+        ov, oi, oit = oracle_rows(oracle.replay, x, k)
         v, i, it, st = api.rtopk_select_stats(xt, k)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        ov, oi, oit = oracle.replay(x[rows], k)
-        assert_same_selection(v, i, ov, oi, rows=rows, what=f"M={M} {value_set} k={k}")
-        np.testing.assert_array_equal(it.cpu().numpy()[rows], oit)
-        _, si = oracle.sort_topk(x[rows], k)
-        np.testing.assert_array_equal(i.cpu().numpy()[rows], si)
+        assert_same_selection(v, i, ov, oi, what=f"M={M} {value_set} k={k} with pass counts")
+        np.testing.assert_array_equal(it.cpu().numpy(), oit)
+        v, i = api.rtopk_select(xt, k)
+        torch.cuda.synchronize()
+        assert_same_selection(v, i, ov, oi, what=f"M={M} {value_set} k={k} default path")
+        del v, i, it, st
+    rows = _sample_rows(N, 300)
+    _, si = oracle.sort_topk(x[rows], 1024)
+    np.testing.assert_array_equal(oi[rows], si)
     del xt
     torch.cuda.empty_cache()
 
@@ -127,9 +144,8 @@ def test_config5_maxk_forward_backward():
     fil = fi.long()
     assert torch.equal(torch.gather(xt, 1, fil).view(torch.int16), fv.view(torch.int16))
     assert bool((fil[:, 1:] > fil[:, :-1]).all()) and int(fil.min()) >= 0 and int(fil.max()) < M
-    rows = _sample_rows(N, 4000)
-    ov, oi, _ = oracle.replay(xb[rows], k)
-    assert_same_selection(fv, fi, ov, oi, rows=rows, what="maxk_forward")
+    ov, oi, _ = oracle_rows(oracle.replay, xb, k)
+    assert_same_selection(fv, fi, ov, oi, what="maxk_forward")
     # backward over all rows against the oracle scatter
     dy = synth.normal_bf16(N, k, seed=1)
     g = api.maxk_backward_scatter(to_dev(dy), fi, M)
@@ -350,3 +366,26 @@ def test_cluster_rows_status_and_neighbours():
     ov, oi, oit = oracle.replay(x[good], k)
     assert_same_selection(v, i, ov, oi, rows=good, what="cluster good rows beside bad ones")
     np.testing.assert_array_equal(it[good], oit)
+
+
+def test_binding_rejects_bad_outputs():
+    """Caller-supplied outputs of the wrong shape, dtype or layout are refused
+    before any launch; a correct one is written in place."""
+    x = to_dev(synth.normal_f32(64, 256, seed=3))
+    with pytest.raises(ValueError):
+        api.rtopk_select(x, 32, vals=torch.empty((64, 31), device="cuda"))
+    with pytest.raises(ValueError):
+        api.rtopk_select(x, 32, idx=torch.empty((64, 32), dtype=torch.int64, device="cuda"))
+    with pytest.raises(ValueError):
+        api.rtopk_select(x, 32, vals=torch.empty((32, 64), device="cuda").t())
+    with pytest.raises(ValueError):
+        api.maxk_backward_scatter(torch.zeros((4, 2), dtype=torch.bfloat16, device="cuda"),
+                                  torch.zeros((4, 2), dtype=torch.int16, device="cuda"), 8,
+                                  grad=torch.empty((4, 7), dtype=torch.bfloat16, device="cuda"))
+    v = torch.empty((64, 32), device="cuda")
+    i = torch.empty((64, 32), dtype=torch.int32, device="cuda")
+    v2, i2 = api.rtopk_select(x, 32, vals=v, idx=i)
+    torch.cuda.synchronize()
+    assert v2.data_ptr() == v.data_ptr() and i2.data_ptr() == i.data_ptr()
+    ov, oi, _ = oracle.replay(x.cpu().numpy(), 32)
+    assert_same_selection(v, i, ov, oi, what="caller-supplied outputs")

@@ -56,15 +56,34 @@ def test_sharded_rows_equal_whole(tmp_path, oracle_mod):
     assert (tmp_path / "ok").read_text() == "1"
 
 
-def test_bench_reference_arm_two_ranks(oracle_mod):
+def _one_json_line(p):
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, p.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_bench_reference_arm_two_ranks_under_torchrun(oracle_mod):
     port = 30500 + (os.getpid() % 1000)
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
-           "--gpus", "2", "--steps", "2", "--warmup", "0", "--rows", "65536"]
-    p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
-    assert p.returncode == 0, p.stderr[-2000:]
-    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
-    assert len(lines) == 1
-    d = json.loads(lines[0])
+           "--gpus", "2", "--steps", "2", "--warmup", "0", "--rows", "65536", "--ref-seconds", "2"]
+    d = _one_json_line(subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600))
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
-    assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["n_gpus"] == 2 and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_bench_gpus_flag_launches_the_ranks_itself(oracle_mod):
+    """`bench.py --gpus 2` without an outer torchrun starts two ranks itself;
+    rank 0 alone prints the line and reports both ranks."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--rows", "65536", "--ref-seconds", "2"]
+    d = _one_json_line(subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600))
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_bench_rejects_a_world_size_that_differs_from_gpus():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=120, env=env)
+    assert p.returncode != 0 and "WORLD_SIZE" in p.stderr
