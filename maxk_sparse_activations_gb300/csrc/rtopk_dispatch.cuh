@@ -6,10 +6,28 @@
 #include "rtopk_block.cuh"
 #include "rtopk_cluster.cuh"
 #include "rtopk_packed.cuh"
+#include "rtopk_lean.cuh"
 
 namespace rtopk {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#ifndef RTOPK_USE_LEAN
+#define RTOPK_USE_LEAN 1
+#endif
+
+// Exact rows of 32 * NE elements without pass counts: the lean kernel
+// (rtopk_lean.cuh).
+template <typename T, int NE, typename IdxT>
+cudaError_t launch_lean(const SelectArgs& a, cudaStream_t s) {
+  constexpr int kThreads = 256;
+  auto kern = lean::rtopk_lean_kernel<T, NE, IdxT>;
+  const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), kThreads, 0, (a.N + 7) / 8);
+  if (blocks <= 0) return cudaErrorInvalidConfiguration;
+  kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.k, static_cast<T*>(a.vals),
+                                   static_cast<IdxT*>(a.idx), a.status);
+  return cudaGetLastError();
+}
 
 // One warp per row (W = 1). L = compaction list entries per lane (0 = off).
 // Measured on GB300 (2^18 N(0,1) rows): compaction costs more than it saves
@@ -24,6 +42,8 @@ cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s
   if constexpr (NE <= 16) {
     // exact mode without pass counts on full rows: the search counts on packed
     // 16-bit images of the row (rtopk_packed.cuh)
+    if (RTOPK_USE_LEAN && exact && a.iters == nullptr && full && a.k <= lean::kListK)
+      return launch_lean<T, NE, IdxT>(a, s);
     if (exact && a.iters == nullptr && full && a.k <= kStageK) {
       auto pk = rtopk_warp_packed_kernel<T, G, IdxT>;
       const int blocks = persistent_blocks(reinterpret_cast<const void*>(pk), kThreads, 0, (a.N + 7) / 8);

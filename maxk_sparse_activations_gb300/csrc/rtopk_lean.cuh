@@ -1,0 +1,512 @@
+// Exact row-wise top-k on rows of 128..512 elements, one warp per row, each
+// lane holding a contiguous slice of the row, the threshold search counted on
+// packed 16-bit images of the row, sm_103a.
+//
+// Source: "RTop-K: Ultra-Fast Row-Wise Top-K Selection for Neural Network
+// Acceleration on GPUs" (summary page), "Approach" (binary search over the
+// row's value range for a threshold that selects k; ties at the threshold
+// filled by the lowest index); CBSR output from "MaxK-GNN: Extremely Fast GPU
+// Kernel Design for Accelerating Graph Neural Networks Training", "The idea".
+//
+// Used for exact mode (max_iter < 0, eps == 0) when per-row pass counts are
+// not requested. The result there is one set -- the k largest values, ties at
+// the k-th value broken by the lowest index -- whatever thresholds the search
+// visits, so it may run on any order-preserving image h of the row: binary16
+// (nearest, saturated at +-65504) for fp32 rows, the data themselves for bf16
+// rows. Over 16-bit thresholds lo < hi with C(lo) >= k > C(hi),
+// C(t) = #{h(x) >= t}:
+//  * C(mid) == k: {h >= mid} is an upper set of the row with k members, the
+//    exact top-k (equal values share an image, so no tie is split);
+//  * no 16-bit value strictly inside (lo, hi): {h >= hi} (< k members) is kept
+//    and the rest of the top-k lies in the bucket {lo <= h < hi}; a binary32
+//    search over the row finishes from [min of the bucket, next binary32 above
+//    its max] (a valid bracket), and the general fill writes the row. bf16
+//    rows whose bracket ends on two adjacent bf16 values go to the fill at once.
+//
+// Instruction budget (the kernel is bound by issue slots, not bytes):
+//  * lane l holds elements [l * NE, (l + 1) * NE): one 256-bit load per lane
+//    for a 1 KB fp32 row, and the kept elements of a lane are consecutive in
+//    index order, so one warp prefix scan of lane counts places them;
+//  * range and precondition: three-input NaN-propagating min / max per lane
+//    and redux.sync on binary32 (max, min, min of the lane maxima);
+//  * the search bracket starts at [image of the smallest lane maximum (k <=
+//    32; each lane holds an element at least that large, so C >= 32 >= k) or
+//    of the row minimum, next 16-bit value above the image of the maximum
+//    (C = 0)]: no test for ties at the maximum is needed;
+//  * a pass compares two elements per set.ge.{f16,bf16}x2 (1.0 or 0.0 per
+//    half), sums up to four compare words per 16-bit field with integer adds
+//    (4 x 1.0 < 2^16 as bit patterns) and folds the two fields with one
+//    dp2a: the lane's count times the bit pattern U of 1.0; one redux.sync
+//    gives U * C(mid), compared with U * k;
+//  * the row's values are copied to shared memory when loaded; the finish
+//    stages only the kept indices (one predicated shared store per element)
+//    and the first k lanes gather values and indices from shared memory and
+//    write the CBSR row with coalesced stores;
+//  * the next row is loaded while the current one is searched, alternating
+//    between two register sets (no copies).
+// Rows whose values are not all finite with |x| <= 1e38 set their status bits
+// and write the row's first k elements (output unspecified, writes in-row).
+#pragma once
+
+#include "rtopk_packed.cuh"
+
+namespace rtopk {
+namespace lean {
+
+constexpr int kListK = 256;  // per-warp list of kept indices (k <= 256)
+
+// ---- small device wrappers -------------------------------------------------
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3_nan(float a, float b, float c) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float warp_max_nan(float v) {
+  float r;
+  asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float warp_min_nan(float v) {
+  float r;
+  asm volatile("redux.sync.min.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// NaN-propagating maximum of a lane's values.
+template <int NE>
+__device__ __forceinline__ float lane_max(const float (&x)[NE]) {
+  float m = x[0];
+  int i = 1;
+#pragma unroll
+  for (; i + 1 < NE; i += 2) m = max3_nan(m, x[i], x[i + 1]);
+  if (i < NE) m = max_nan(m, x[i]);
+  return m;
+}
+// ---- 16-bit image traits ----------------------------------------------------
+template <typename T>
+struct Img;
+template <>
+struct Img<float> {
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t min2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+};
+template <>
+struct Img<uint16_t> {
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ uint32_t min2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+};
+
+// Next 16-bit value above the (splat) image word w, in both halves: +-0 ->
+// smallest positive subnormal, positive -> +1 ulp, negative -> toward zero.
+// The image of a valid fp32 maximum is at most 65504, whose successor is
+// +inf; the search then collapses at once and the binary32 finish takes the
+// whole bucket.
+__device__ __forceinline__ uint32_t next_up16(uint32_t w) {
+  const uint32_t b = w & 0xffffu;
+  const uint32_t nb = (b & 0x7fffu) == 0u ? 1u : ((b & 0x8000u) ? b - 1u : b + 1u);
+  return nb | (nb << 16);
+}
+
+// ---- loads and lane layout ---------------------------------------------------
+// RW 32-bit words of input per lane: NE for fp32, NE / 2 for bf16.
+template <typename T, int NE>
+struct Lane {
+  static constexpr int RW = sizeof(T) == 4 ? NE : NE / 2;
+  static constexpr int W = NE / 2;  // packed image words
+};
+
+// Asynchronous copy of one row (32 * RW words) into a shared stage: lane l
+// copies the 16-byte chunks l, l + 32, ... (coalesced), so the stage holds the
+// row in element order. dst_lane / src_lane already point at the lane's first
+// chunk. One commit group per row.
+template <int RW>
+__device__ __forceinline__ void issue_row(uint32_t dst_lane, const uint32_t* __restrict__ src_lane, bool valid) {
+#pragma unroll
+  for (int c = 0; c < RW / 4; ++c) {
+    if (valid)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_lane + uint32_t(c * 512)),
+                   "l"(src_lane + c * 128)
+                   : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int PENDING>
+__device__ __forceinline__ void wait_rows() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
+}
+
+// The lane's RW consecutive words [lane * RW, (lane + 1) * RW) of a staged row.
+template <int RW>
+__device__ __forceinline__ void lane_words(const uint32_t* __restrict__ srow, int lane, uint32_t (&w)[RW]) {
+#pragma unroll
+  for (int i = 0; i < RW; i += 4) {
+    const uint4 q = *reinterpret_cast<const uint4*>(srow + lane * RW + i);
+    w[i] = q.x; w[i + 1] = q.y; w[i + 2] = q.z; w[i + 3] = q.w;
+  }
+}
+
+// Binary32 values of the lane's elements from its raw words.
+template <typename T, int NE>
+__device__ __forceinline__ void widen(const uint32_t (&w)[Lane<T, NE>::RW], float (&x)[NE]) {
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    if constexpr (sizeof(T) == 4) {
+      x[e] = __uint_as_float(w[e]);
+    } else {  // element 2q in the low half of word q (lower address)
+      x[e] = (e & 1) ? __uint_as_float(w[e / 2] & 0xffff0000u) : __uint_as_float(w[e / 2] << 16);
+    }
+  }
+}
+
+// The lane's values again, from the shared copy of the row (rare paths: the
+// row's registers are not kept alive through the search for them).
+template <typename T, int NE>
+__device__ __forceinline__ void reload(const uint32_t* __restrict__ srow, int lane, float (&x)[NE]) {
+  uint32_t w[Lane<T, NE>::RW];
+  lane_words<Lane<T, NE>::RW>(srow, lane, w);
+  widen<T, NE>(w, x);
+}
+
+// ---- finishes ---------------------------------------------------------------
+// Kept indices of the exact ending C(t) == k, from that pass's compares s[]:
+// this lane's kept elements go to list positions [ex, ex + count) in index
+// order; one predicated shared store per element.
+template <int W>
+__device__ __forceinline__ void stage_exact(const uint32_t (&s)[W], uint32_t c, int lane, uint32_t list_addr) {
+  uint32_t incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1)
+    asm("{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+        "shfl.sync.up.b32 t|p, %0, %1, 0, -1;\n\t"
+        "@p add.u32 %0, %0, t;\n\t}"
+        : "+r"(incl) : "r"(d));
+  uint32_t a = list_addr + (incl - c) * 4u;
+  const uint32_t j0 = uint32_t(lane) * uint32_t(2 * W);
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+        "and.b32 t, %1, 65535;\n\t"
+        "setp.ne.u32 p, t, 0;\n\t"
+        "@p st.shared.u32 [%0], %2;\n\t"
+        "@p add.u32 %0, %0, 4;\n\t}"
+        : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ge.u32 p, %1, 65536;\n\t"
+        "@p st.shared.u32 [%0], %2;\n\t"
+        "@p add.u32 %0, %0, 4;\n\t}"
+        : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w + 1u) : "memory");
+  }
+}
+
+// General fill for a binary32 bracket [lo, hi) with c(lo) >= k > c(hi): keep
+// every x >= hi, then the first k - c(hi) of lo <= x < hi in index order.
+template <int NE>
+__device__ __forceinline__ void stage_general(const float (&x)[NE], float lo, float hi, int k, int lane,
+                                              uint32_t* __restrict__ list) {
+  uint32_t sc = 0, bc = 0;
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    const bool s = x[e] >= hi;
+    sc += s ? 1u : 0u;
+    bc += (!s && x[e] >= lo) ? 1u : 0u;
+  }
+  uint32_t incl = sc | (bc << 16);
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+  const uint32_t ex = incl - (sc | (bc << 16));
+  const int need = k - int(tot & 0xffffu);
+  int bpos = int(ex >> 16);
+  int pos = int(ex & 0xffffu) + min(bpos, need);
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    const bool s = x[e] >= hi;
+    const bool b = !s && x[e] >= lo;
+    if (s || (b && bpos < need)) {
+      list[pos] = uint32_t(lane * NE + e);
+      ++pos;
+    }
+    bpos += b ? 1 : 0;
+  }
+}
+
+// CBSR row from the staged list: value bits gathered from the staged row,
+// indices as listed (ascending). vrow / irow point at the row's k outputs.
+template <typename T, typename IdxT>
+__device__ __forceinline__ void copy_out(const uint32_t* __restrict__ list, const uint32_t* __restrict__ srow,
+                                         int k, int lane, T* __restrict__ vrow, IdxT* __restrict__ irow) {
+  __syncwarp();
+  auto one = [&](int p) {
+    const uint32_t j = list[p];
+    T v;
+    if constexpr (sizeof(T) == 4) {
+      v = __uint_as_float(srow[j]);
+    } else {
+      v = reinterpret_cast<const uint16_t*>(srow)[j];
+    }
+    vrow[p] = v;
+    irow[p] = IdxT(j);
+  };
+  if (k <= 32) {
+    if (lane < k) one(lane);
+  } else {
+    for (int p = lane; p < k; p += 32) one(p);
+  }
+  __syncwarp();
+}
+
+// Exact binary32 search from a valid bracket [lo, hi] (c(lo) >= k > c(hi)),
+// then the general fill. Used inside the last 16-bit bucket (and for the
+// rare bf16 bracket that ends on two non-adjacent values).
+template <int NE>
+__device__ __forceinline__ void finish_binary32(const float (&x)[NE], float lo, float hi, int k, int lane,
+                                                uint32_t* __restrict__ list, uint32_t& st) {
+  int it = 0;
+  for (;; ++it) {
+    const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
+    if (!(lo < mid && mid < hi)) break;
+    if (it >= kSafetyCap) {
+      st |= kStatusSafetyCap;
+      break;
+    }
+    uint32_t c = 0;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) c += (x[e] >= mid) ? 1u : 0u;
+    const int cnt = int(warp_sum(c));
+    if (cnt >= k) lo = mid;
+    else hi = mid;
+    if (cnt == k) break;
+  }
+  stage_general<NE>(x, lo, hi, k, lane, list);
+}
+
+// ---- one row ------------------------------------------------------------------
+template <typename T, int NE, typename IdxT>
+__device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, int k, int lane,
+                                            uint32_t* __restrict__ list, T* __restrict__ vrow,
+                                            IdxT* __restrict__ irow, uint32_t& st) {
+  using P = Packed16<T>;
+  using I = Img<T>;
+  constexpr int RW = Lane<T, NE>::RW;
+  constexpr int W = Lane<T, NE>::W;
+  constexpr unsigned FULL = 0xffffffffu;
+  uint32_t raw[RW];
+  lane_words<RW>(srow, lane, raw);
+
+  // ---- image, range and precondition. hi32 bounds every |x| (fp32) or x
+  // (bf16) from above; lo_src is a value with at least k elements >= it.
+  uint32_t h[W];
+  float hi32, lo_src;
+  bool valid;
+  if constexpr (sizeof(T) == 4) {
+    float x[NE];
+    widen<T, NE>(raw, x);
+#pragma unroll
+    for (int w = 0; w < W; ++w) h[w] = P::pack(x[2 * w + 1], x[2 * w]);
+    float a = fabsf(x[0]);
+    int i = 1;
+#pragma unroll
+    for (; i + 1 < NE; i += 2) a = max3_nan(a, fabsf(x[i]), fabsf(x[i + 1]));
+    if (i < NE) a = max_nan(a, fabsf(x[i]));
+    hi32 = warp_max_nan(a);  // NaN if any element is NaN
+    valid = hi32 <= 1e38f;
+    // k <= 32: each of the 32 lanes holds an element >= its maximum
+    lo_src = (k <= 32) ? warp_min_nan(lane_max<NE>(x)) : -hi32;
+  } else {
+#pragma unroll
+    for (int w = 0; w < W; ++w) h[w] = raw[w];
+    uint32_t m = h[0], n = h[0];
+#pragma unroll
+    for (int w = 1; w < W; ++w) {
+      m = I::max2(m, h[w]);
+      n = I::min2(n, h[w]);
+    }
+    m = I::max2(m, __byte_perm(m, 0, 0x1032));  // both halves: the lane maximum
+    n = I::min2(n, __byte_perm(n, 0, 0x1032));
+    const float mx = __uint_as_float(m & 0xffff0000u);
+    hi32 = warp_max_nan(mx);
+    const float lo_row = warp_min_nan(__uint_as_float(n & 0xffff0000u));
+    valid = hi32 <= 1e38f && lo_row >= -1e38f;
+    lo_src = (k <= 32) ? warp_min_nan(mx) : lo_row;
+  }
+  if (!valid) {
+    // invalid row: report which precondition fails, write the first k elements
+    float x[NE];
+    reload<T, NE>(srow, lane, x);
+    bool nonfinite = false, range = false;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      const float a = fabsf(x[e]);
+      nonfinite |= !(a <= 3.402823466e38f);
+      range |= (a > 1e38f && a <= 3.402823466e38f);
+    }
+    if (__any_sync(FULL, nonfinite)) st |= kStatusNonFinite;
+    if (__any_sync(FULL, range)) st |= kStatusRange;
+    for (int p = lane; p < k; p += 32) list[p] = uint32_t(p);
+    copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+    return;
+  }
+
+  // ---- coarse bisection on 16-bit images: C(lo2) >= k > C(hi2) = 0
+  uint32_t lo2 = P::splat(lo_src);
+  uint32_t hi2 = next_up16(P::splat(hi32));
+  const uint32_t k0 = uint32_t(k) << 16, k1 = uint32_t(k + 1) << 16;
+  const uint32_t list_addr = static_cast<uint32_t>(__cvta_generic_to_shared(list));
+  // One pass: s[w] = (h[w] >= m2) per half (1.0 or 0.0); the lane's count,
+  // accumulated from 1024.0 (binary16) / 128.0 (bf16) where the spacing is 1,
+  // folded to bits 16..31 by one multiply-add; the warp sum of those words.
+  auto pass = [&](uint32_t m2, uint32_t (&s)[W], uint32_t& u) {
+    uint32_t acc = P::kMagic2;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      s[w] = P::set_ge(h[w], m2);
+      acc = P::add(acc, s[w]);
+    }
+    u = acc * 0x10001u - P::kFold;  // (c_hi + c_lo) << 16 | c_lo
+    return warp_sum(u);
+  };
+  // Two passes per iteration, the collapse test on the first: the midpoint
+  // always lies in [lo, hi] (as a value), so no 16-bit value strictly inside
+  // means it equals lo or hi; after a collapse the second pass counts at lo
+  // or hi, leaves the bracket as it is, and the next test ends the search. A
+  // midpoint of the other signed zero than lo / hi passes the test and costs
+  // one pass at the same value.
+  for (;;) {
+    uint32_t m2 = P::midpoint(lo2, hi2);
+    if (m2 == lo2 || m2 == hi2) break;
+    uint32_t sa[W], ua;
+    uint32_t tot = pass(m2, sa, ua);
+    bool ge = tot >= k0;
+    if (ge && tot < k1) {
+      stage_exact<W>(sa, ua >> 16, lane, list_addr);
+      copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+      return;
+    }
+    lo2 = ge ? m2 : lo2;
+    hi2 = ge ? hi2 : m2;
+    m2 = P::midpoint(lo2, hi2);
+    uint32_t sb[W], ub;
+    tot = pass(m2, sb, ub);
+    ge = tot >= k0;
+    if (ge && tot < k1) {
+      stage_exact<W>(sb, ub >> 16, lane, list_addr);
+      copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+      return;
+    }
+    lo2 = ge ? m2 : lo2;
+    hi2 = ge ? hi2 : m2;
+  }
+
+  // ---- collapsed: the rest of the top-k lies in the bucket {lo <= h < hi}
+  float x[NE];
+  reload<T, NE>(srow, lane, x);
+  const float lo = P::low_f32(lo2), hi = P::low_f32(hi2);
+  if (sizeof(T) == 2 && next_up_bf16(lo) == hi) {
+    // bf16: the bucket holds one value (every x in it equals lo)
+    stage_general<NE>(x, lo, hi, k, lane, list);
+  } else {
+    float bmin = pos_inf(), bmax = neg_inf();
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float hl = P::low_f32(h[w]), hh = P::high_f32(h[w]);
+      const bool il = hl >= lo && !(hl >= hi);
+      const bool ih = hh >= lo && !(hh >= hi);
+      bmin = fminf(bmin, il ? x[2 * w] : pos_inf());
+      bmax = fmaxf(bmax, il ? x[2 * w] : neg_inf());
+      bmin = fminf(bmin, ih ? x[2 * w + 1] : pos_inf());
+      bmax = fmaxf(bmax, ih ? x[2 * w + 1] : neg_inf());
+    }
+    const float flo = o2f(__reduce_min_sync(FULL, f2o(bmin)));
+    const float fhi = next_up_f32(o2f(__reduce_max_sync(FULL, f2o(bmax))));
+    finish_binary32<NE>(x, flo, fhi, k, lane, list, st);
+  }
+  copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+}
+
+#ifndef RTOPK_LEAN_MIN_BLOCKS
+#define RTOPK_LEAN_MIN_BLOCKS 5
+#endif
+// Rows in flight per warp (shared stages) and resident blocks of 256 per SM.
+template <int NE>
+struct LeanCfg {
+  static constexpr int kStages = NE <= 8 ? 3 : 2;
+  static constexpr int kBlocks = NE <= 8 ? RTOPK_LEAN_MIN_BLOCKS : 3;
+};
+
+// Full rows of 32 * NE elements, exact mode, k <= kListK, 16-byte aligned.
+// One warp per row, persistent over rows; each warp keeps kStages rows in
+// flight through cp.async copies into its own shared stages.
+template <typename T, int NE, typename IdxT>
+__global__ void __launch_bounds__(256, LeanCfg<NE>::kBlocks)
+rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ vals, IdxT* __restrict__ idx,
+                  uint32_t* __restrict__ status) {
+  constexpr int RW = Lane<T, NE>::RW;
+  constexpr int S = LeanCfg<NE>::kStages;
+  constexpr int kRowWords = 32 * RW;
+  __shared__ __align__(16) uint32_t ring_all[8][S][kRowWords];
+  __shared__ uint32_t list_all[8][kListK];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  uint32_t* list = list_all[wib];
+  const int64_t nw = int64_t(gridDim.x) * 8;
+  const int64_t r0 = int64_t(blockIdx.x) * 8 + wib;
+  const int nrows = r0 < N ? int((N - 1 - r0) / nw) + 1 : 0;  // rows r0, r0 + nw, ... < N
+  constexpr uint32_t kStageBytes = uint32_t(kRowWords) * 4u;
+  const uint32_t ring_lane = static_cast<uint32_t>(__cvta_generic_to_shared(ring_all[wib][0])) + uint32_t(lane * 16);
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(in) + r0 * kRowWords + lane * 4;  // next row to issue
+  const int64_t src_step = nw * kRowWords;
+  uint32_t st = 0;
+  // prologue: the warp's first S rows
+#pragma unroll
+  for (int q = 0; q < S; ++q) {
+    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, q < nrows);
+    src += src_step;
+  }
+  T* vrow = vals + r0 * int64_t(k);
+  IdxT* irow = idx + r0 * int64_t(k);
+  const int64_t out_step = nw * int64_t(k);
+  int q = 0;
+  for (int i = 0; i < nrows; ++i) {
+    wait_rows<S - 1>();  // this row's copy group is complete
+    __syncwarp();
+    process_row<T, NE, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
+    // process_row ends with __syncwarp: every lane is done with this stage
+    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, i + S < nrows);
+    src += src_step;
+    vrow += out_step;
+    irow += out_step;
+    q = (q + 1 == S) ? 0 : q + 1;
+  }
+  wait_rows<0>();
+  if (status != nullptr && st != 0u && lane == 0) atomicOr(status, st);
+}
+
+}  // namespace lean
+}  // namespace rtopk
