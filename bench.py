@@ -74,7 +74,7 @@ def algorithmic_bytes(N, M, k, s_in, s_val, s_idx):
 
 # sources that define the timed kernel (fp32 rows of <= 2048 elements, one warp per row)
 # and its launch configuration
-HEADLINE_SOURCES = ("rtopk_device.cuh", "rtopk_select.cuh", "rtopk_warp.cuh", "rtopk_packed.cuh", "rtopk_block.cuh",
+HEADLINE_SOURCES = ("rtopk_device.cuh", "rtopk_select.cuh", "rtopk_warp.cuh", "rtopk_image16.cuh", "rtopk_lean.cuh", "rtopk_block.cuh",
                     "rtopk_dispatch.cuh", "rtopk_f32.cu", "launch_util.cu")
 
 

@@ -5,16 +5,11 @@
 #include "rtopk_select.cuh"
 #include "rtopk_block.cuh"
 #include "rtopk_cluster.cuh"
-#include "rtopk_packed.cuh"
 #include "rtopk_lean.cuh"
 
 namespace rtopk {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-#ifndef RTOPK_USE_LEAN
-#define RTOPK_USE_LEAN 1
-#endif
 
 // Exact rows of 32 * NE elements without pass counts: the lean kernel
 // (rtopk_lean.cuh).
@@ -40,18 +35,9 @@ cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s
   constexpr int NE = G * ElemTraits<T>::V;
   const bool exact = a.max_iter < 0 && a.eps == 0.0f;
   if constexpr (NE <= 16) {
-    // exact mode without pass counts on full rows: the search counts on packed
-    // 16-bit images of the row (rtopk_packed.cuh)
-    if (RTOPK_USE_LEAN && exact && a.iters == nullptr && full && a.k <= lean::kListK)
-      return launch_lean<T, NE, IdxT>(a, s);
-    if (exact && a.iters == nullptr && full && a.k <= kStageK) {
-      auto pk = rtopk_warp_packed_kernel<T, G, IdxT>;
-      const int blocks = persistent_blocks(reinterpret_cast<const void*>(pk), kThreads, 0, (a.N + 7) / 8);
-      if (blocks <= 0) return cudaErrorInvalidConfiguration;
-      pk<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.M, a.k, static_cast<T*>(a.vals),
-                                     static_cast<IdxT*>(a.idx), a.status);
-      return cudaGetLastError();
-    }
+    // exact mode without pass counts on full rows: the search counts on
+    // packed 16-bit images of the row (rtopk_lean.cuh)
+    if (exact && a.iters == nullptr && full && a.k <= lean::kListK) return launch_lean<T, NE, IdxT>(a, s);
   }
   const int L = (NE >= 64 && a.k <= 128) ? 8 : ((NE >= 32 && a.k <= 64) ? 4 : 0);
   using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);
@@ -107,6 +93,11 @@ cudaError_t launch_short_rows(const SelectArgs& a, cudaStream_t s) {
   constexpr int GS = 32 * V;
   const int M = a.M;
   const bool vec = (M % V == 0) && aligned16(a.in);
+  if constexpr (sizeof(T) == 2) {
+    // bf16 rows of 128 (4 per lane, 8 bytes): the lean kernel in exact mode
+    if (M == 128 && vec && a.max_iter < 0 && a.eps == 0.0f && a.iters == nullptr && a.k <= lean::kListK)
+      return launch_lean<T, 4, IdxT>(a, s);
+  }
   const int need = (M + GS - 1) / GS;
   const int G = need <= 4 ? need : (need <= 6 ? 6 : (need <= 8 ? 8 : (need <= 12 ? 12 : 16)));
   const bool full = vec && M == G * GS;

@@ -23,32 +23,36 @@
 //    its max] (a valid bracket), and the general fill writes the row. bf16
 //    rows whose bracket ends on two adjacent bf16 values go to the fill at once.
 //
-// Instruction budget (the kernel is bound by issue slots, not bytes):
-//  * lane l holds elements [l * NE, (l + 1) * NE): one 256-bit load per lane
-//    for a 1 KB fp32 row, and the kept elements of a lane are consecutive in
-//    index order, so one warp prefix scan of lane counts places them;
-//  * range and precondition: three-input NaN-propagating min / max per lane
-//    and redux.sync on binary32 (max, min, min of the lane maxima);
+// Design (the search, not the bytes, bounds the kernel: measured on GB300 at
+// 2^20 x 256 fp32, k = 32, the same kernel without the search runs at 0.94 of
+// the HBM copy bandwidth, with it at 0.61; the search passes load the
+// half-rate ALU and FMA-heavy pipes about equally, so the compares are summed
+// with fp16 adds and the lane fold is one integer multiply-add):
+//  * lane l holds elements [l * NE, (l + 1) * NE), so the kept elements of a
+//    lane are consecutive in index order and one warp prefix scan of lane
+//    counts places them;
+//  * rows stream through a ring of shared-memory stages per warp (cp.async,
+//    coalesced 16-byte chunks, kStages rows in flight); a lane reads its slice
+//    from the stage, and the stage is also the source of the CBSR values;
+//  * range and precondition: NaN-propagating three-input max of |x| per lane
+//    and redux.sync on binary32 (fp32 rows); packed bf16x2 max / min (bf16);
 //  * the search bracket starts at [image of the smallest lane maximum (k <=
-//    32; each lane holds an element at least that large, so C >= 32 >= k) or
-//    of the row minimum, next 16-bit value above the image of the maximum
-//    (C = 0)]: no test for ties at the maximum is needed;
+//    32: each lane holds an element at least that large, so C >= 32 >= k) or
+//    of a row lower bound, next 16-bit value above the image of the upper
+//    bound (C = 0)]: no test for ties at the maximum is needed;
 //  * a pass compares two elements per set.ge.{f16,bf16}x2 (1.0 or 0.0 per
-//    half), sums up to four compare words per 16-bit field with integer adds
-//    (4 x 1.0 < 2^16 as bit patterns) and folds the two fields with one
-//    dp2a: the lane's count times the bit pattern U of 1.0; one redux.sync
-//    gives U * C(mid), compared with U * k;
-//  * the row's values are copied to shared memory when loaded; the finish
-//    stages only the kept indices (one predicated shared store per element)
-//    and the first k lanes gather values and indices from shared memory and
-//    write the CBSR row with coalesced stores;
-//  * the next row is loaded while the current one is searched, alternating
-//    between two register sets (no copies).
+//    half), adds them to 1024.0 (binary16) / 128.0 (bf16), where the spacing
+//    is 1, so the field bits read offset + count, and one integer multiply-add
+//    folds both halves into bits 16..31; one redux.sync sums the lanes;
+//  * the finish stages only the kept indices (one predicated shared store per
+//    element); the first k lanes gather values and indices and write the CBSR
+//    row with coalesced stores.
 // Rows whose values are not all finite with |x| <= 1e38 set their status bits
 // and write the row's first k elements (output unspecified, writes in-row).
 #pragma once
 
-#include "rtopk_packed.cuh"
+#include "rtopk_image16.cuh"
+#include "rtopk_select.cuh"
 
 namespace rtopk {
 namespace lean {
@@ -142,10 +146,12 @@ struct Lane {
 // row in element order. dst_lane / src_lane already point at the lane's first
 // chunk. One commit group per row.
 template <int RW>
-__device__ __forceinline__ void issue_row(uint32_t dst_lane, const uint32_t* __restrict__ src_lane, bool valid) {
+__device__ __forceinline__ void issue_row(uint32_t dst_lane, const uint32_t* __restrict__ src_lane, int lane,
+                                          bool valid) {
+  constexpr int CH = 8 * RW;  // 16-byte chunks per row
 #pragma unroll
-  for (int c = 0; c < RW / 4; ++c) {
-    if (valid)
+  for (int c = 0; c < (CH + 31) / 32; ++c) {
+    if (valid && (CH % 32 == 0 || lane + 32 * c < CH))
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_lane + uint32_t(c * 512)),
                    "l"(src_lane + c * 128)
                    : "memory");
@@ -160,10 +166,16 @@ __device__ __forceinline__ void wait_rows() {
 // The lane's RW consecutive words [lane * RW, (lane + 1) * RW) of a staged row.
 template <int RW>
 __device__ __forceinline__ void lane_words(const uint32_t* __restrict__ srow, int lane, uint32_t (&w)[RW]) {
+  if constexpr (RW % 4 == 0) {
 #pragma unroll
-  for (int i = 0; i < RW; i += 4) {
-    const uint4 q = *reinterpret_cast<const uint4*>(srow + lane * RW + i);
-    w[i] = q.x; w[i + 1] = q.y; w[i + 2] = q.z; w[i + 3] = q.w;
+    for (int i = 0; i < RW; i += 4) {
+      const uint4 q = *reinterpret_cast<const uint4*>(srow + lane * RW + i);
+      w[i] = q.x; w[i + 1] = q.y; w[i + 2] = q.z; w[i + 3] = q.w;
+    }
+  } else {
+    static_assert(RW == 2, "8-byte lane slices");
+    const uint2 q = *reinterpret_cast<const uint2*>(srow + lane * RW);
+    w[0] = q.x; w[1] = q.y;
   }
 }
 
@@ -392,36 +404,35 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
     u = acc * 0x10001u - P::kFold;  // (c_hi + c_lo) << 16 | c_lo
     return warp_sum(u);
   };
-  // Two passes per iteration, the collapse test on the first: the midpoint
-  // always lies in [lo, hi] (as a value), so no 16-bit value strictly inside
-  // means it equals lo or hi; after a collapse the second pass counts at lo
-  // or hi, leaves the bracket as it is, and the next test ends the search. A
-  // midpoint of the other signed zero than lo / hi passes the test and costs
-  // one pass at the same value.
+  // Two passes per collapse test: the midpoint always lies in [lo, hi] (as a
+  // value), so no 16-bit value strictly inside means it equals lo or hi; after
+  // a collapse the second pass counts at lo or hi, leaves the bracket as it
+  // is, and the next test ends the search. A midpoint of the other signed zero
+  // than lo / hi passes the test and costs one pass at the same value. Every
+  // pass keeps its own compares and, on C == k, writes the row from them where
+  // it ends (one exit per pass: a single shared exit measured slower).
+  // Measured on GB300 (2^20 x 256 fp32, k = 32) and not kept: a test every 3
+  // or 4 passes, a pairwise-sum tree, bracket updates as integer multiply-adds
+  // (off the ALU pipe), a bracket top from the warp maximum instead of max |x|,
+  // and a row loop unrolled over the ring stages -- each 1-20% slower.
   for (;;) {
     uint32_t m2 = P::midpoint(lo2, hi2);
     if (m2 == lo2 || m2 == hi2) break;
-    uint32_t sa[W], ua;
-    uint32_t tot = pass(m2, sa, ua);
-    bool ge = tot >= k0;
-    if (ge && tot < k1) {
-      stage_exact<W>(sa, ua >> 16, lane, list_addr);
-      copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
-      return;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j > 0) m2 = P::midpoint(lo2, hi2);
+      uint32_t s[W], u;
+      const uint32_t tot = pass(m2, s, u);
+      const bool ge = tot >= k0;
+      if (ge && tot < k1) {
+        // C(mid) == k: {h >= mid} is the top-k
+        stage_exact<W>(s, u >> 16, lane, list_addr);
+        copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+        return;
+      }
+      lo2 = ge ? m2 : lo2;
+      hi2 = ge ? hi2 : m2;
     }
-    lo2 = ge ? m2 : lo2;
-    hi2 = ge ? hi2 : m2;
-    m2 = P::midpoint(lo2, hi2);
-    uint32_t sb[W], ub;
-    tot = pass(m2, sb, ub);
-    ge = tot >= k0;
-    if (ge && tot < k1) {
-      stage_exact<W>(sb, ub >> 16, lane, list_addr);
-      copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
-      return;
-    }
-    lo2 = ge ? m2 : lo2;
-    hi2 = ge ? hi2 : m2;
   }
 
   // ---- collapsed: the rest of the top-k lies in the bucket {lo <= h < hi}
@@ -486,7 +497,7 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
   // prologue: the warp's first S rows
 #pragma unroll
   for (int q = 0; q < S; ++q) {
-    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, q < nrows);
+    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, lane, q < nrows);
     src += src_step;
   }
   T* vrow = vals + r0 * int64_t(k);
@@ -498,7 +509,7 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
     __syncwarp();
     process_row<T, NE, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
     // process_row ends with __syncwarp: every lane is done with this stage
-    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, i + S < nrows);
+    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, lane, i + S < nrows);
     src += src_step;
     vrow += out_step;
     irow += out_step;

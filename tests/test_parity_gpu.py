@@ -389,3 +389,25 @@ def test_binding_rejects_bad_outputs():
     assert v2.data_ptr() == v.data_ptr() and i2.data_ptr() == i.data_ptr()
     ov, oi, _ = oracle.replay(x.cpu().numpy(), 32)
     assert_same_selection(v, i, ov, oi, what="caller-supplied outputs")
+
+
+@pytest.mark.parametrize("M,k", [(256, 32), (256, 16), (512, 64), (128, 8), (2048, 256), (64, 12), (1024, 40)])
+def test_backward_group_shapes(M, k):
+    """The backward scatter's row groups: partial last group, 16-byte and
+    2-byte pair loads, a bad index in the last group (flagged, skipped, the
+    rest of the output exact)."""
+    N = 8 * 3 + 5
+    rng = np.random.default_rng(M + k)
+    idx = np.sort(np.stack([rng.choice(M, size=k, replace=False) for _ in range(N)]), axis=1).astype(np.int16)
+    dy = synth.normal_bf16(N, k, seed=7)
+    g = api.maxk_backward_scatter(to_dev(dy), torch.from_numpy(idx).cuda(), M)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(vals_np(g), oracle.maxk_backward(dy, idx, M))
+    bad = idx.copy()
+    bad[N - 2, k // 2] = M + 3  # out of range
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = api.maxk_backward_scatter(to_dev(dy), torch.from_numpy(bad).cuda(), M, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 0x8
+    ok = np.setdiff1d(np.arange(N), [N - 2])
+    np.testing.assert_array_equal(vals_np(g)[ok], oracle.maxk_backward(dy[ok], idx[ok], M))
