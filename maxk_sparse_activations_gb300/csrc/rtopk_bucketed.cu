@@ -6,13 +6,18 @@
 //
 // A row of M elements is split into B contiguous buckets of M / B; each bucket
 // keeps its own top-(k / B) under the same selection as rtopk_select (exact by
-// default, or early-stopped). Viewed as (N * B) rows of M / B elements, the
-// matrix and the CBSR output already have the layout of that smaller problem,
-// so the selection kernels run unchanged; one pass then turns bucket-local
-// column indices into row indices (+ bucket * M / B). Buckets are in column
-// order and each bucket's indices ascend, so every output row ascends.
+// default, or early-stopped).
+//  * Exact mode on full rows of 128..512 (B = 2, 4, 8): the lean kernel with
+//    the row's B buckets on B lane groups of one warp, searched side by side
+//    (rtopk_lean.cuh, process_row_bucketed); indices come out as row columns.
+//  * Otherwise: viewed as (N * B) rows of M / B elements, the matrix and the
+//    CBSR output already have the layout of the smaller problem, so the
+//    selection kernels run unchanged; one pass then turns bucket-local column
+//    indices into row indices (+ bucket * M / B). Buckets are in column order
+//    and each bucket's indices ascend, so every output row ascends.
 #include <cstdint>
 
+#include "rtopk_lean.cuh"
 #include "launch.h"
 
 namespace rtopk {
@@ -27,9 +32,54 @@ bucket_index_offset_kernel(int32_t* __restrict__ idx, int64_t total, int kb, int
   }
 }
 
+template <typename T, int NE, int B>
+cudaError_t launch_lean_bucketed(const SelectArgs& a, cudaStream_t s) {
+  auto kern = lean::rtopk_lean_kernel<T, NE, int32_t, B>;
+  const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), 256, 0, (a.N + 7) / 8);
+  if (blocks <= 0) return cudaErrorInvalidConfiguration;
+  kern<<<blocks, 256, 0, s>>>(static_cast<const T*>(a.in), a.N, a.k, static_cast<T*>(a.vals),
+                              static_cast<int32_t*>(a.idx), a.status);
+  return cudaGetLastError();
+}
+
+template <typename T, int NE>
+cudaError_t launch_lean_b(const SelectArgs& a, int buckets, cudaStream_t s) {
+  switch (buckets) {
+    case 2: return launch_lean_bucketed<T, NE, 2>(a, s);
+    case 4: return launch_lean_bucketed<T, NE, 4>(a, s);
+    default: return launch_lean_bucketed<T, NE, 8>(a, s);
+  }
+}
+
+// Exact mode, B in {2, 4, 8}, rows of 32 * NE elements (NE the lean kernel's
+// slice sizes), 16-byte aligned: returns true and launches.
+bool try_lean_bucketed(const SelectArgs& a, bool bf16, int buckets, cudaStream_t s, cudaError_t& err) {
+  const bool exact = a.max_iter < 0 && a.eps == 0.0f;
+  if (!exact || a.iters != nullptr || a.k > lean::kListK) return false;
+  if (buckets != 2 && buckets != 4 && buckets != 8) return false;
+  if ((reinterpret_cast<uintptr_t>(a.in) & 15u) != 0) return false;
+  if (bf16) {
+    switch (a.M) {
+      case 128: err = launch_lean_b<uint16_t, 4>(a, buckets, s); return true;
+      case 256: err = launch_lean_b<uint16_t, 8>(a, buckets, s); return true;
+      case 512: err = launch_lean_b<uint16_t, 16>(a, buckets, s); return true;
+      default: return false;
+    }
+  }
+  switch (a.M) {
+    case 128: err = launch_lean_b<float, 4>(a, buckets, s); return true;
+    case 256: err = launch_lean_b<float, 8>(a, buckets, s); return true;
+    case 384: err = launch_lean_b<float, 12>(a, buckets, s); return true;
+    case 512: err = launch_lean_b<float, 16>(a, buckets, s); return true;
+    default: return false;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select_bucketed(const SelectArgs& a, int dtype_bf16, int buckets, cudaStream_t s) {
+  cudaError_t err = cudaSuccess;
+  if (buckets > 1 && try_lean_bucketed(a, dtype_bf16 != 0, buckets, s, err)) return err;
   SelectArgs b = a;
   b.N = a.N * buckets;
   b.M = a.M / buckets;

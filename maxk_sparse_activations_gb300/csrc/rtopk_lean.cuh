@@ -235,16 +235,18 @@ __device__ __forceinline__ void stage_exact(const uint32_t (&s)[W], uint32_t c, 
 }
 
 // General fill for a binary32 bracket [lo, hi) with c(lo) >= k > c(hi): keep
-// every x >= hi, then the first k - c(hi) of lo <= x < hi in index order.
+// every x >= hi, then the first k - c(hi) of lo <= x < hi in index order, at
+// list positions [base, base + k). Lanes with `active` false hold none of the
+// elements concerned (a bucket of lanes selects on its own).
 template <int NE>
 __device__ __forceinline__ void stage_general(const float (&x)[NE], float lo, float hi, int k, int lane,
-                                              uint32_t* __restrict__ list) {
+                                              uint32_t* __restrict__ list, bool active = true, int base = 0) {
   uint32_t sc = 0, bc = 0;
 #pragma unroll
   for (int e = 0; e < NE; ++e) {
-    const bool s = x[e] >= hi;
+    const bool s = active && x[e] >= hi;
     sc += s ? 1u : 0u;
-    bc += (!s && x[e] >= lo) ? 1u : 0u;
+    bc += (active && !s && x[e] >= lo) ? 1u : 0u;
   }
   uint32_t incl = sc | (bc << 16);
 #pragma unroll
@@ -256,11 +258,11 @@ __device__ __forceinline__ void stage_general(const float (&x)[NE], float lo, fl
   const uint32_t ex = incl - (sc | (bc << 16));
   const int need = k - int(tot & 0xffffu);
   int bpos = int(ex >> 16);
-  int pos = int(ex & 0xffffu) + min(bpos, need);
+  int pos = base + int(ex & 0xffffu) + min(bpos, need);
 #pragma unroll
   for (int e = 0; e < NE; ++e) {
-    const bool s = x[e] >= hi;
-    const bool b = !s && x[e] >= lo;
+    const bool s = active && x[e] >= hi;
+    const bool b = active && !s && x[e] >= lo;
     if (s || (b && bpos < need)) {
       list[pos] = uint32_t(lane * NE + e);
       ++pos;
@@ -299,7 +301,8 @@ __device__ __forceinline__ void copy_out(const uint32_t* __restrict__ list, cons
 // rare bf16 bracket that ends on two non-adjacent values).
 template <int NE>
 __device__ __forceinline__ void finish_binary32(const float (&x)[NE], float lo, float hi, int k, int lane,
-                                                uint32_t* __restrict__ list, uint32_t& st) {
+                                                uint32_t* __restrict__ list, uint32_t& st, bool active = true,
+                                                int base = 0) {
   int it = 0;
   for (;; ++it) {
     const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
@@ -310,13 +313,13 @@ __device__ __forceinline__ void finish_binary32(const float (&x)[NE], float lo, 
     }
     uint32_t c = 0;
 #pragma unroll
-    for (int e = 0; e < NE; ++e) c += (x[e] >= mid) ? 1u : 0u;
+    for (int e = 0; e < NE; ++e) c += (active && x[e] >= mid) ? 1u : 0u;
     const int cnt = int(warp_sum(c));
     if (cnt >= k) lo = mid;
     else hi = mid;
     if (cnt == k) break;
   }
-  stage_general<NE>(x, lo, hi, k, lane, list);
+  stage_general<NE>(x, lo, hi, k, lane, list, active, base);
 }
 
 // ---- one row ------------------------------------------------------------------
@@ -461,6 +464,176 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
   copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
 }
 
+// ---- one row split into B buckets ------------------------------------------------
+// "Approximate Top-k for Increased Parallelism" (abstract): each bucket of a
+// row keeps its own top-(k / B) independently. With M = 32 * NE, bucket b is
+// the columns of lanes [b * LB, (b + 1) * LB), LB = 32 / B, so the B searches
+// run side by side in one warp: each lane holds its bucket's bracket, a pass
+// compares every lane against its bucket's midpoint, and the bucket counts
+// come from one redux.sync over fields of 32 / B bits (B <= 4; a bucket count
+// is at most LB * NE < 2^(32 / B)) or an LB-lane butterfly (B >= 8). The
+// loop runs until every bucket has found its threshold or collapsed. The
+// buckets are in column order and each keeps exactly k / B, so the warp-wide
+// placement of the kept elements is the bucketed CBSR row, indices already
+// row columns. A bucket whose search ends on tied 16-bit images finishes with
+// an exact binary32 search inside its last bracket, bucket by bucket.
+template <int LB>
+__device__ __forceinline__ float seg_max_nan(float v) {
+#pragma unroll
+  for (int d = LB / 2; d >= 1; d >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+template <int LB>
+__device__ __forceinline__ float seg_min_nan(float v) {
+#pragma unroll
+  for (int d = LB / 2; d >= 1; d >>= 1) v = min_nan(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+// Sum of c over the lanes of bucket b (every lane of the warp calls it).
+template <int B>
+__device__ __forceinline__ uint32_t bucket_sum(uint32_t c, int b) {
+  constexpr int LB = 32 / B;
+  if constexpr (B <= 4) {
+    constexpr int FW = 32 / B;
+    const uint32_t tot = warp_sum(c << (FW * b));
+    return FW == 32 ? tot : ((tot >> (FW * b)) & ((1u << (FW & 31)) - 1u));
+  } else {
+#pragma unroll
+    for (int d = LB / 2; d >= 1; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    return c;
+  }
+}
+
+template <typename T, int NE, int B, typename IdxT>
+__device__ __forceinline__ void process_row_bucketed(const uint32_t* __restrict__ srow, int k, int lane,
+                                                     uint32_t* __restrict__ list, T* __restrict__ vrow,
+                                                     IdxT* __restrict__ irow, uint32_t& st) {
+  using P = Packed16<T>;
+  using I = Img<T>;
+  constexpr int RW = Lane<T, NE>::RW;
+  constexpr int W = Lane<T, NE>::W;
+  constexpr int LB = 32 / B;
+  constexpr unsigned FULL = 0xffffffffu;
+  const int b = lane / LB;
+  const int kb = k / B;
+  uint32_t raw[RW];
+  lane_words<RW>(srow, lane, raw);
+  uint32_t h[W];
+  float mx, mn;
+  if constexpr (sizeof(T) == 4) {
+    float x[NE];
+    widen<T, NE>(raw, x);
+#pragma unroll
+    for (int w = 0; w < W; ++w) h[w] = P::pack(x[2 * w + 1], x[2 * w]);
+    mx = lane_max<NE>(x);
+    float m = x[0];
+#pragma unroll
+    for (int e = 1; e < NE; ++e) m = min_nan(m, x[e]);
+    mn = m;
+  } else {
+#pragma unroll
+    for (int w = 0; w < W; ++w) h[w] = raw[w];
+    uint32_t m = h[0], n = h[0];
+#pragma unroll
+    for (int w = 1; w < W; ++w) {
+      m = I::max2(m, h[w]);
+      n = I::min2(n, h[w]);
+    }
+    mx = __uint_as_float(I::max2(m, __byte_perm(m, 0, 0x1032)) & 0xffff0000u);
+    mn = __uint_as_float(I::min2(n, __byte_perm(n, 0, 0x1032)) & 0xffff0000u);
+  }
+  const float row_hi = warp_max_nan(mx), row_lo = warp_min_nan(mn);
+  if (!(row_hi <= 1e38f && row_lo >= -1e38f)) {
+    float x[NE];
+    reload<T, NE>(srow, lane, x);
+    bool nonfinite = false, range = false;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      const float a = fabsf(x[e]);
+      nonfinite |= !(a <= 3.402823466e38f);
+      range |= (a > 1e38f && a <= 3.402823466e38f);
+    }
+    if (__any_sync(FULL, nonfinite)) st |= kStatusNonFinite;
+    if (__any_sync(FULL, range)) st |= kStatusRange;
+    for (int p = lane; p < k; p += 32) list[p] = uint32_t(p);
+    copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+    return;
+  }
+  // bucket brackets: [image of the smallest lane maximum (kb <= LB) or of the
+  // bucket minimum, next 16-bit value above the image of the bucket maximum]
+  const float top = seg_max_nan<LB>(mx);
+  const float lo_b = seg_min_nan<LB>(kb <= LB ? mx : mn);
+  uint32_t lo2 = P::splat(lo_b);
+  uint32_t hi2 = next_up16(P::splat(top));
+  // Branch-free per bucket: once no 16-bit value lies strictly inside the
+  // bracket (the midpoint equals lo or hi), the pass counts at lo; if C == k / B
+  // there the bucket's threshold is found (this catches a starting lower end
+  // that already holds exactly k / B elements), else the bucket is done
+  // unresolved (tied images at its k/B-th value). A finished bucket keeps its
+  // bracket (lo = its threshold when found).
+  bool done = false, exact = false;
+  for (;;) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t mid = P::midpoint(lo2, hi2);
+      const bool coll = mid == lo2 || mid == hi2;
+      const uint32_t m2 = coll ? lo2 : mid;
+      uint32_t acc = P::kMagic2;
+#pragma unroll
+      for (int w = 0; w < W; ++w) acc = P::add(acc, P::set_ge(h[w], m2));
+      const int cb = int(bucket_sum<B>((acc * 0x10001u - P::kFold) >> 16, b));
+      const bool hit = cb == kb, ge = cb >= kb;
+      lo2 = (!done && ge) ? m2 : lo2;
+      hi2 = (!done && !ge) ? m2 : hi2;
+      exact = exact || (!done && hit);
+      done = done || hit || coll;
+    }
+    if (__all_sync(FULL, done)) break;
+  }
+  // Buckets with a threshold: their kept sets {h >= lo} placed in one pass.
+  // An unresolved bucket reserves its k / B list positions (its first lane
+  // counts k / B, its lanes store nothing) and is finished below.
+  uint32_t sw[W];
+  uint32_t acc = P::kMagic2;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    sw[w] = exact ? P::set_ge(h[w], lo2) : 0u;
+    acc = P::add(acc, sw[w]);
+  }
+  const uint32_t cl = exact ? (acc * 0x10001u - P::kFold) >> 16 : ((lane % LB) == 0 ? uint32_t(kb) : 0u);
+  stage_exact<W>(sw, cl, lane, static_cast<uint32_t>(__cvta_generic_to_shared(list)));
+  const unsigned open = __ballot_sync(FULL, !exact);
+  if (open != 0u) {
+    // unresolved buckets (tied images at the k/B-th value): exact binary32
+    // search inside the bucket's last 16-bit bracket {lo <= h < hi}, then the
+    // general fill at the bucket's list positions
+    __syncwarp();
+    float x[NE];
+    reload<T, NE>(srow, lane, x);
+    const float lo = P::low_f32(lo2), hi = P::low_f32(hi2);
+    float bmin = pos_inf(), bmax = neg_inf();
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float hl = P::low_f32(h[w]), hh = P::high_f32(h[w]);
+      const bool il = hl >= lo && !(hl >= hi);
+      const bool ih = hh >= lo && !(hh >= hi);
+      bmin = fminf(bmin, il ? x[2 * w] : pos_inf());
+      bmax = fmaxf(bmax, il ? x[2 * w] : neg_inf());
+      bmin = fminf(bmin, ih ? x[2 * w + 1] : pos_inf());
+      bmax = fmaxf(bmax, ih ? x[2 * w + 1] : neg_inf());
+    }
+#pragma unroll 1
+    for (int bs = 0; bs < B; ++bs) {
+      if (!((open >> (bs * LB)) & 1u)) continue;  // warp-uniform
+      const bool act = b == bs;
+      const float flo = o2f(__reduce_min_sync(FULL, f2o(act ? bmin : pos_inf())));
+      const float fhi = next_up_f32(o2f(__reduce_max_sync(FULL, f2o(act ? bmax : neg_inf()))));
+      finish_binary32<NE>(x, flo, fhi, kb, lane, list, st, act, bs * kb);
+    }
+  }
+  copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+}
+
 #ifndef RTOPK_LEAN_MIN_BLOCKS
 #define RTOPK_LEAN_MIN_BLOCKS 5
 #endif
@@ -471,10 +644,11 @@ struct LeanCfg {
   static constexpr int kBlocks = NE <= 8 ? RTOPK_LEAN_MIN_BLOCKS : 3;
 };
 
-// Full rows of 32 * NE elements, exact mode, k <= kListK, 16-byte aligned.
-// One warp per row, persistent over rows; each warp keeps kStages rows in
-// flight through cp.async copies into its own shared stages.
-template <typename T, int NE, typename IdxT>
+// Full rows of 32 * NE elements, exact mode, k <= kListK, 16-byte aligned
+// (B > 1: B buckets per row, B dividing 32 and k). One warp per row,
+// persistent over rows; each warp keeps kStages rows in flight through
+// cp.async copies into its own shared stages.
+template <typename T, int NE, typename IdxT, int B = 1>
 __global__ void __launch_bounds__(256, LeanCfg<NE>::kBlocks)
 rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ vals, IdxT* __restrict__ idx,
                   uint32_t* __restrict__ status) {
@@ -507,7 +681,11 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
   for (int i = 0; i < nrows; ++i) {
     wait_rows<S - 1>();  // this row's copy group is complete
     __syncwarp();
-    process_row<T, NE, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
+    if constexpr (B == 1) {
+      process_row<T, NE, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
+    } else {
+      process_row_bucketed<T, NE, B, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
+    }
     // process_row ends with __syncwarp: every lane is done with this stage
     issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, lane, i + S < nrows);
     src += src_step;

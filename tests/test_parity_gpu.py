@@ -411,3 +411,25 @@ def test_backward_group_shapes(M, k):
     assert int(st.item()) & 0x8
     ok = np.setdiff1d(np.arange(N), [N - 2])
     np.testing.assert_array_equal(vals_np(g)[ok], oracle.maxk_backward(dy[ok], idx[ok], M))
+
+
+@pytest.mark.parametrize("value_set", ["normal", "int_ties", "dense_bucket", "subnormal", "all_equal",
+                                       "wide_range", "signed_zeros"])
+@pytest.mark.parametrize("dtype,M", [("f32", 128), ("f32", 256), ("f32", 384), ("f32", 512),
+                                     ("bf16", 128), ("bf16", 256), ("bf16", 512)])
+def test_bucketed_exact_side_by_side_buckets(value_set, dtype, M):
+    """Exact bucketed top-k where one warp searches all buckets of a row side
+    by side (B in {2, 4, 8}): every row against the oracle, on value sets that
+    make buckets collapse (ties, rows inside one 16-bit bucket) so the
+    bucket-by-bucket binary32 finish runs too."""
+    N = 500
+    x = synth.make(value_set, N, M, seed=M + 3, dtype=dtype)
+    xt = to_dev(x)
+    for B in (2, 4, 8):
+        for k in sorted({B, 4 * B, 8 * B, 16 * B, 32 * B}):
+            if k > M or k > 256:
+                continue
+            v, i = api.rtopk_select_bucketed(xt, k, B)
+            torch.cuda.synchronize()
+            ov, oi = oracle.bucketed_topk(x, k, B)
+            assert_same_selection(v, i, ov, oi, what=f"bucketed {value_set} {dtype} M={M} B={B} k={k}")
