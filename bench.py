@@ -449,7 +449,7 @@ def run_gb300(args, rank: int, world: int):
                          "frac": gbs / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                          else "fallback", "algorithmic_bytes_per_launch": bytes_step,
-                         "kernel": "rtopk_warp_packed_kernel<float,G=2,int32>",
+                         "kernel": "rtopk_lean_kernel<float,NE=8,int32>",
                          "traffic_source": os.path.relpath(prof, ROOT) if prof else None},
             "cpu_baseline": cpu,
             "e2e": {"value": world * N_ROWS / (ms_e2e * 1e-3), "unit": "rows/s",
@@ -712,8 +712,36 @@ def _case_maxk_forward():
         api.maxk_forward(xb, 32)
 
 
+def _case_maxk_backward():
+    # the MaxK backward of the fused-layer workload at a quarter of its rows:
+    # 2^18 rows, k = 32 bf16 gradients at the forward's int16 indices -> dense
+    # 2^18 x 256 bf16 gradient (128 MB written)
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    n, M, k = 1 << 18, 256, 32
+    xb = torch.from_numpy(synth.normal_bf16(n, M, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    _, fi = api.maxk_forward(xb, k)
+    dy = torch.from_numpy(synth.normal_bf16(n, k, seed=1).view(np.int16)).view(torch.bfloat16).to(dev)
+    g = torch.empty((n, M), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        api.maxk_backward_scatter(dy, fi, M, grad=g)
+
+
+def _case_bucketed():
+    # bucketed top-k, B = 4, on a quarter of the headline matrix: 2^18 x 256
+    # fp32 N(0,1), k = 32 (268 MB in)
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    x = torch.from_numpy(synth.normal_f32(1 << 18, 256, seed=0)).to(dev)
+    for _ in range(3):
+        api.rtopk_select_bucketed(x, 32, 4)
+
+
 PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward,
-                 "maxk-forward": _case_maxk_forward}
+                 "maxk-forward": _case_maxk_forward, "maxk-backward": _case_maxk_backward,
+                 "bucketed": _case_bucketed}
 
 
 def run_case(name: str) -> int:

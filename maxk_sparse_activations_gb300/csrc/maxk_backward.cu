@@ -100,6 +100,9 @@ maxk_backward_warp_kernel(const uint16_t* __restrict__ dy, const int16_t* __rest
       }
     }
   };
+  // VEC: k % 8 == 0, so a lane's 8 entries [8 l, 8 l + 8) lie in one row of
+  // every group; its offset in the group block is fixed
+  const int vrow_off = VEC ? ((lane * EP) / k) * M : 0;
   fetch(g);
   for (; g < ngroups; g += nw) {
     int16_t cc[EP];
@@ -117,9 +120,9 @@ maxk_backward_warp_kernel(const uint16_t* __restrict__ dy, const int16_t* __rest
     for (int q = 0; q < EP; ++q) {
       const int e = VEC ? lane * EP + q : lane + 32 * q;
       if (e < nec) {
-        const int row = e / k;
+        const int off = VEC ? vrow_off : (e / k) * M;
         if (cc[q] >= 0 && cc[q] < M) {
-          buf[row * M + cc[q]] = vv[q];
+          buf[off + cc[q]] = vv[q];
         } else {
           st |= kStatusBadIndex;
         }
