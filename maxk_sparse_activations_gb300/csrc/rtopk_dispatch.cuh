@@ -11,6 +11,10 @@ namespace rtopk {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+#ifndef RTOPK_LEAN_NE_MAX
+#define RTOPK_LEAN_NE_MAX 32  // elements per lane of the largest rows the lean kernel takes
+#endif
+
 // Exact rows of 32 * NE elements without pass counts: the lean kernel
 // (rtopk_lean.cuh).
 template <typename T, int NE, typename IdxT>
@@ -34,7 +38,7 @@ cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s
   constexpr int kThreads = 256;
   constexpr int NE = G * ElemTraits<T>::V;
   const bool exact = a.max_iter < 0 && a.eps == 0.0f;
-  if constexpr (NE <= 16) {
+  if constexpr (NE <= RTOPK_LEAN_NE_MAX) {
     // exact mode without pass counts on full rows: the search counts on
     // packed 16-bit images of the row (rtopk_lean.cuh)
     if (exact && a.iters == nullptr && full && a.k <= lean::kListK) return launch_lean<T, NE, IdxT>(a, s);

@@ -1,4 +1,4 @@
-// Exact row-wise top-k on rows of 128..512 elements, one warp per row, each
+// Exact row-wise top-k on rows of 128..1024 elements, one warp per row, each
 // lane holding a contiguous slice of the row, the threshold search counted on
 // packed 16-bit images of the row, sm_103a.
 //
@@ -58,6 +58,10 @@ namespace rtopk {
 namespace lean {
 
 constexpr int kListK = 256;  // per-warp list of kept indices (k <= 256)
+
+#ifndef RTOPK_LEAN_SWZ
+#define RTOPK_LEAN_SWZ 1
+#endif
 
 // ---- small device wrappers -------------------------------------------------
 __device__ __forceinline__ float max3_nan(float a, float b, float c) {
@@ -141,20 +145,62 @@ struct Lane {
   static constexpr int W = NE / 2;  // packed image words
 };
 
-// Asynchronous copy of one row (32 * RW words) into a shared stage: lane l
-// copies the 16-byte chunks l, l + 32, ... (coalesced), so the stage holds the
-// row in element order. dst_lane / src_lane already point at the lane's first
-// chunk. One commit group per row.
+// Layout of a row in its shared stage, in 16-byte chunks. Lane L's slice is
+// chunks [L * CPL, (L + 1) * CPL). When CPL is 4 or 8 the eight lanes of a
+// shared-memory phase would read the same banks (slices 64 or 128 bytes
+// apart: 4- / 8-way conflicts), so chunk c of lane L is stored at
+// L * CPL + (c ^ s(L)), s(L) the lane bits the stride folds onto one bank
+// group: every lane's chunk c then sits in its own bank group (GB300, 2^18
+// rows of 1024 fp32: 385 -> 233 us at k = 16). Other slices keep the row in
+// element order (a 2-chunk swizzle measured slower: its 2-way conflicts cost
+// less than the address arithmetic).
 template <int RW>
-__device__ __forceinline__ void issue_row(uint32_t dst_lane, const uint32_t* __restrict__ src_lane, int lane,
+struct StageLayout {
+  static constexpr int CPL = RW >= 4 ? RW / 4 : 1;  // 16-byte chunks per lane
+  static constexpr int SH = CPL == 4 ? 1 : 0;
+  static constexpr bool SWZ = RTOPK_LEAN_SWZ && (CPL == 4 || CPL == 8);
+  static __device__ __forceinline__ int chunk_pos(int L, int c) {
+    if constexpr (SWZ) {
+      return L * CPL + (c ^ ((L >> SH) & (CPL - 1)));
+    } else {
+      return L * CPL + c;
+    }
+  }
+  // word offset in the stage of element j (4-byte elements: 4 per chunk)
+  static __device__ __forceinline__ int word_of_f32(int j) {
+    if constexpr (SWZ) {
+      const int g = j >> 2;
+      return chunk_pos(g / CPL, g % CPL) * 4 + (j & 3);
+    } else {
+      return j;
+    }
+  }
+  // 16-bit offset in the stage of element j (2-byte elements: 8 per chunk)
+  static __device__ __forceinline__ int half_of_bf16(int j) {
+    if constexpr (SWZ) {
+      const int g = j >> 3;
+      return chunk_pos(g / CPL, g % CPL) * 8 + (j & 7);
+    } else {
+      return j;
+    }
+  }
+};
+
+// Asynchronous copy of one row (32 * RW words) into a shared stage: lane l
+// copies the 16-byte chunks l, l + 32, ... of the row (coalesced) to their
+// stage positions. One commit group per row.
+template <int RW>
+__device__ __forceinline__ void issue_row(uint32_t stage, const uint32_t* __restrict__ src_lane, int lane,
                                           bool valid) {
+  using SL = StageLayout<RW>;
   constexpr int CH = 8 * RW;  // 16-byte chunks per row
 #pragma unroll
-  for (int c = 0; c < (CH + 31) / 32; ++c) {
-    if (valid && (CH % 32 == 0 || lane + 32 * c < CH))
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_lane + uint32_t(c * 512)),
-                   "l"(src_lane + c * 128)
-                   : "memory");
+  for (int i = 0; i < (CH + 31) / 32; ++i) {
+    const int g = lane + 32 * i;
+    const uint32_t dst = SL::SWZ ? stage + uint32_t(SL::chunk_pos(g / SL::CPL, g % SL::CPL)) * 16u
+                                 : stage + uint32_t(lane * 16 + i * 512);
+    if (valid && (CH % 32 == 0 || g < CH))
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src_lane + i * 128) : "memory");
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -163,14 +209,15 @@ __device__ __forceinline__ void wait_rows() {
   asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
 }
 
-// The lane's RW consecutive words [lane * RW, (lane + 1) * RW) of a staged row.
+// The lane's RW consecutive words (elements [lane * NE, (lane + 1) * NE)) of a
+// staged row.
 template <int RW>
 __device__ __forceinline__ void lane_words(const uint32_t* __restrict__ srow, int lane, uint32_t (&w)[RW]) {
   if constexpr (RW % 4 == 0) {
 #pragma unroll
-    for (int i = 0; i < RW; i += 4) {
-      const uint4 q = *reinterpret_cast<const uint4*>(srow + lane * RW + i);
-      w[i] = q.x; w[i + 1] = q.y; w[i + 2] = q.z; w[i + 3] = q.w;
+    for (int c = 0; c < RW / 4; ++c) {
+      const uint4 q = *reinterpret_cast<const uint4*>(srow + StageLayout<RW>::chunk_pos(lane, c) * 4);
+      w[4 * c] = q.x; w[4 * c + 1] = q.y; w[4 * c + 2] = q.z; w[4 * c + 3] = q.w;
     }
   } else {
     static_assert(RW == 2, "8-byte lane slices");
@@ -273,17 +320,18 @@ __device__ __forceinline__ void stage_general(const float (&x)[NE], float lo, fl
 
 // CBSR row from the staged list: value bits gathered from the staged row,
 // indices as listed (ascending). vrow / irow point at the row's k outputs.
-template <typename T, typename IdxT>
+template <typename T, int RW, typename IdxT>
 __device__ __forceinline__ void copy_out(const uint32_t* __restrict__ list, const uint32_t* __restrict__ srow,
                                          int k, int lane, T* __restrict__ vrow, IdxT* __restrict__ irow) {
+  using SL = StageLayout<RW>;
   __syncwarp();
   auto one = [&](int p) {
     const uint32_t j = list[p];
     T v;
     if constexpr (sizeof(T) == 4) {
-      v = __uint_as_float(srow[j]);
+      v = __uint_as_float(srow[SL::word_of_f32(int(j))]);
     } else {
-      v = reinterpret_cast<const uint16_t*>(srow)[j];
+      v = reinterpret_cast<const uint16_t*>(srow)[SL::half_of_bf16(int(j))];
     }
     vrow[p] = v;
     irow[p] = IdxT(j);
@@ -385,7 +433,7 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
     if (__any_sync(FULL, nonfinite)) st |= kStatusNonFinite;
     if (__any_sync(FULL, range)) st |= kStatusRange;
     for (int p = lane; p < k; p += 32) list[p] = uint32_t(p);
-    copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+    copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
     return;
   }
 
@@ -430,7 +478,7 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
       if (ge && tot < k1) {
         // C(mid) == k: {h >= mid} is the top-k
         stage_exact<W>(s, u >> 16, lane, list_addr);
-        copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+        copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
         return;
       }
       lo2 = ge ? m2 : lo2;
@@ -461,7 +509,7 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
     const float fhi = next_up_f32(o2f(__reduce_max_sync(FULL, f2o(bmax))));
     finish_binary32<NE>(x, flo, fhi, k, lane, list, st);
   }
-  copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+  copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
 }
 
 // ---- one row split into B buckets ------------------------------------------------
@@ -556,7 +604,7 @@ __device__ __forceinline__ void process_row_bucketed(const uint32_t* __restrict_
     if (__any_sync(FULL, nonfinite)) st |= kStatusNonFinite;
     if (__any_sync(FULL, range)) st |= kStatusRange;
     for (int p = lane; p < k; p += 32) list[p] = uint32_t(p);
-    copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+    copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
     return;
   }
   // bucket brackets: [image of the smallest lane maximum (kb <= LB) or of the
@@ -631,17 +679,22 @@ __device__ __forceinline__ void process_row_bucketed(const uint32_t* __restrict_
       finish_binary32<NE>(x, flo, fhi, kb, lane, list, st, act, bs * kb);
     }
   }
-  copy_out<T, IdxT>(list, srow, k, lane, vrow, irow);
+  copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
 }
 
 #ifndef RTOPK_LEAN_MIN_BLOCKS
 #define RTOPK_LEAN_MIN_BLOCKS 5
 #endif
 // Rows in flight per warp (shared stages) and resident blocks of 256 per SM.
-template <int NE>
+// Rows of 1024 fp32 (128 bytes per lane): 2 blocks (72 KB of stages each, 80+
+// registers; at 3 blocks the kernel spills); measured on GB300 at 2^18 rows:
+// 224-333 us at 2 blocks against 233-343 us at 3 (k = 16..256), bf16 rows of
+// 1024 the other way round (234-367 against 250-392 us).
+template <typename T, int NE>
 struct LeanCfg {
   static constexpr int kStages = NE <= 8 ? 3 : 2;
-  static constexpr int kBlocks = NE <= 8 ? RTOPK_LEAN_MIN_BLOCKS : 3;
+  static constexpr int kBlocks =
+      NE <= 8 ? RTOPK_LEAN_MIN_BLOCKS : ((NE >= 32 && sizeof(T) == 4) ? 2 : 3);
 };
 
 // Full rows of 32 * NE elements, exact mode, k <= kListK, 16-byte aligned
@@ -649,11 +702,11 @@ struct LeanCfg {
 // persistent over rows; each warp keeps kStages rows in flight through
 // cp.async copies into its own shared stages.
 template <typename T, int NE, typename IdxT, int B = 1>
-__global__ void __launch_bounds__(256, LeanCfg<NE>::kBlocks)
+__global__ void __launch_bounds__(256, LeanCfg<T, NE>::kBlocks)
 rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ vals, IdxT* __restrict__ idx,
                   uint32_t* __restrict__ status) {
   constexpr int RW = Lane<T, NE>::RW;
-  constexpr int S = LeanCfg<NE>::kStages;
+  constexpr int S = LeanCfg<T, NE>::kStages;
   constexpr int kRowWords = 32 * RW;
   __shared__ __align__(16) uint32_t ring_all[8][S][kRowWords];
   __shared__ uint32_t list_all[8][kListK];
@@ -664,14 +717,14 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
   const int64_t r0 = int64_t(blockIdx.x) * 8 + wib;
   const int nrows = r0 < N ? int((N - 1 - r0) / nw) + 1 : 0;  // rows r0, r0 + nw, ... < N
   constexpr uint32_t kStageBytes = uint32_t(kRowWords) * 4u;
-  const uint32_t ring_lane = static_cast<uint32_t>(__cvta_generic_to_shared(ring_all[wib][0])) + uint32_t(lane * 16);
+  const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring_all[wib][0]));
   const uint32_t* src = reinterpret_cast<const uint32_t*>(in) + r0 * kRowWords + lane * 4;  // next row to issue
   const int64_t src_step = nw * kRowWords;
   uint32_t st = 0;
   // prologue: the warp's first S rows
 #pragma unroll
   for (int q = 0; q < S; ++q) {
-    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, lane, q < nrows);
+    issue_row<RW>(ring_base + uint32_t(q) * kStageBytes, src, lane, q < nrows);
     src += src_step;
   }
   T* vrow = vals + r0 * int64_t(k);
@@ -687,7 +740,7 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
       process_row_bucketed<T, NE, B, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
     }
     // process_row ends with __syncwarp: every lane is done with this stage
-    issue_row<RW>(ring_lane + uint32_t(q) * kStageBytes, src, lane, i + S < nrows);
+    issue_row<RW>(ring_base + uint32_t(q) * kStageBytes, src, lane, i + S < nrows);
     src += src_step;
     vrow += out_step;
     irow += out_step;

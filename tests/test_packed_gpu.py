@@ -34,7 +34,7 @@ def _gpu():
 
 
 @pytest.mark.parametrize("value_set", VALUE_SETS)
-@pytest.mark.parametrize("M", [128, 256, 384, 512])
+@pytest.mark.parametrize("M", [128, 256, 384, 512, 768, 1024])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_packed_exact_is_the_definition(value_set, M, dtype):
     N = 400
