@@ -7,10 +7,10 @@
 // whatever thresholds the bisection visits, so it may count on any
 // order-preserving image of the row (x <= y implies h(x) <= h(y)).
 //
-// Counting detail: a per-lane accumulator starting at 1024.0 (binary16) or
-// 128.0 (bf16) in both halves, where the spacing is 1, takes one 1.0 per kept
-// element exactly, so the field bits read (offset + count); one integer
-// multiply-add (x 0x10001, minus kFold) folds both halves into bits 16..31.
+// Operations: the bracket midpoint lo * 0.5 + (hi * 0.5) (one rounding, always
+// in [lo, hi], odd-symmetric: the midpoint of the negated ends is the negated
+// midpoint), packed adds, splats of a binary32 value, and the halves widened
+// back to binary32.
 #pragma once
 
 #include <cstdint>
@@ -32,8 +32,6 @@ struct Packed16<float> {
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(lo2), "r"(kHalf2), "r"(t));
     return d;
   }
-  static constexpr uint32_t kMagic2 = 0x64006400u;  // 1024.0 in both halves
-  static constexpr uint32_t kFold = 0xc8006400u;     // (2 * 0x6400 << 16) + 0x6400
   // both halves = round-to-nearest binary16 of v, saturated at +-65504
   static __device__ __forceinline__ uint32_t splat(float v) {
     uint32_t d;
@@ -56,11 +54,6 @@ struct Packed16<float> {
     asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, u;\n\t}" : "=f"(f) : "r"(w));
     return f;
   }
-  static __device__ __forceinline__ uint32_t set_ge(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("set.ge.f16x2.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
   static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -79,8 +72,6 @@ struct Packed16<uint16_t> {
     asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(lo2), "r"(kHalf2), "r"(t));
     return d;
   }
-  static constexpr uint32_t kMagic2 = 0x43004300u;  // 128.0 in both halves
-  static constexpr uint32_t kFold = 0x86004300u;     // (2 * 0x4300 << 16) + 0x4300
   static __device__ __forceinline__ uint32_t splat(float v) {
     uint32_t d;
     asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(v));
@@ -91,11 +82,6 @@ struct Packed16<uint16_t> {
   }
   static __device__ __forceinline__ float low_f32(uint32_t w) { return __uint_as_float(w << 16); }
   static __device__ __forceinline__ float high_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-  static __device__ __forceinline__ uint32_t set_ge(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("set.ge.bf16x2.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
   static __device__ __forceinline__ uint32_t add(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

@@ -26,8 +26,8 @@
 // Design (the search, not the bytes, bounds the kernel: measured on GB300 at
 // 2^20 x 256 fp32, k = 32, the same kernel without the search runs at 0.94 of
 // the HBM copy bandwidth, with it at 0.61; the search passes load the
-// half-rate ALU and FMA-heavy pipes about equally, so the compares are summed
-// with fp16 adds and the lane fold is one integer multiply-add):
+// half-rate ALU and FMA-heavy pipes about equally, so the compares run as
+// fp16 subtractions and the counting as byte sums):
 //  * lane l holds elements [l * NE, (l + 1) * NE), so the kept elements of a
 //    lane are consecutive in index order and one warp prefix scan of lane
 //    counts places them;
@@ -40,10 +40,9 @@
 //    32: each lane holds an element at least that large, so C >= 32 >= k) or
 //    of a row lower bound, next 16-bit value above the image of the upper
 //    bound (C = 0)]: no test for ties at the maximum is needed;
-//  * a pass compares two elements per set.ge.{f16,bf16}x2 (1.0 or 0.0 per
-//    half), adds them to 1024.0 (binary16) / 128.0 (bf16), where the spacing
-//    is 1, so the field bits read offset + count, and one integer multiply-add
-//    folds both halves into bits 16..31; one redux.sync sums the lanes;
+//  * a pass forms h - t for two elements per packed add (FMA pipe), gathers
+//    the sign bits of four halves into sign-replicated bytes with one prmt and
+//    adds them with dp4a (the lane's negatives); one redux.sync sums the lanes;
 //  * the finish stages only the kept indices (one predicated shared store per
 //    element); the first k lanes gather values and indices and write the CBSR
 //    row with coalesced stores.
@@ -85,6 +84,19 @@ __device__ __forceinline__ float warp_min_nan(float v) {
   return r;
 }
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xffffffffu, v); }
+// The sign bits of the four 16-bit halves of a and b, each replicated over a
+// byte (0xff for a negative half): prmt with the sign-replicate selector bit.
+__device__ __forceinline__ uint32_t half_signs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, 0xFDB9;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// c + the four bytes of a as signed integers (each 0 or -1 here)
+__device__ __forceinline__ int sum_bytes(uint32_t a, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x01010101), "r"(c));
+  return d;
+}
 
 // NaN-propagating maximum of a lane's values.
 template <int NE>
@@ -252,7 +264,9 @@ __device__ __forceinline__ void reload(const uint32_t* __restrict__ srow, int la
 // Kept indices of the exact ending C(t) == k, from that pass's compares s[]:
 // this lane's kept elements go to list positions [ex, ex + count) in index
 // order; one predicated shared store per element.
-template <int W>
+// SIGN: s[w] holds h - t per half (kept when the sign bit is clear) instead
+// of the 1.0 / 0.0 compare results.
+template <int W, bool SIGN = false>
 __device__ __forceinline__ void stage_exact(const uint32_t (&s)[W], uint32_t c, int lane, uint32_t list_addr) {
   uint32_t incl = c;
 #pragma unroll
@@ -265,19 +279,35 @@ __device__ __forceinline__ void stage_exact(const uint32_t (&s)[W], uint32_t c, 
   const uint32_t j0 = uint32_t(lane) * uint32_t(2 * W);
 #pragma unroll
   for (int w = 0; w < W; ++w) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
-        "and.b32 t, %1, 65535;\n\t"
-        "setp.ne.u32 p, t, 0;\n\t"
-        "@p st.shared.u32 [%0], %2;\n\t"
-        "@p add.u32 %0, %0, 4;\n\t}"
-        : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w) : "memory");
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ge.u32 p, %1, 65536;\n\t"
-        "@p st.shared.u32 [%0], %2;\n\t"
-        "@p add.u32 %0, %0, 4;\n\t}"
-        : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w + 1u) : "memory");
+    if constexpr (SIGN) {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+          "and.b32 t, %1, 32768;\n\t"
+          "setp.eq.u32 p, t, 0;\n\t"
+          "@p st.shared.u32 [%0], %2;\n\t"
+          "@p add.u32 %0, %0, 4;\n\t}"
+          : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w) : "memory");
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "setp.ge.s32 p, %1, 0;\n\t"
+          "@p st.shared.u32 [%0], %2;\n\t"
+          "@p add.u32 %0, %0, 4;\n\t}"
+          : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w + 1u) : "memory");
+    } else {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t.reg .u32 t;\n\t"
+          "and.b32 t, %1, 65535;\n\t"
+          "setp.ne.u32 p, t, 0;\n\t"
+          "@p st.shared.u32 [%0], %2;\n\t"
+          "@p add.u32 %0, %0, 4;\n\t}"
+          : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w) : "memory");
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "setp.ge.u32 p, %1, 65536;\n\t"
+          "@p st.shared.u32 [%0], %2;\n\t"
+          "@p add.u32 %0, %0, 4;\n\t}"
+          : "+r"(a) : "r"(s[w]), "r"(j0 + 2u * w + 1u) : "memory");
+    }
   }
 }
 
@@ -440,51 +470,63 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
   // ---- coarse bisection on 16-bit images: C(lo2) >= k > C(hi2) = 0
   uint32_t lo2 = P::splat(lo_src);
   uint32_t hi2 = next_up16(P::splat(hi32));
-  const uint32_t k0 = uint32_t(k) << 16, k1 = uint32_t(k + 1) << 16;
   const uint32_t list_addr = static_cast<uint32_t>(__cvta_generic_to_shared(list));
-  // One pass: s[w] = (h[w] >= m2) per half (1.0 or 0.0); the lane's count,
-  // accumulated from 1024.0 (binary16) / 128.0 (bf16) where the spacing is 1,
-  // folded to bits 16..31 by one multiply-add; the warp sum of those words.
-  auto pass = [&](uint32_t m2, uint32_t (&s)[W], uint32_t& u) {
-    uint32_t acc = P::kMagic2;
+  // A pass forms d = h - t per half with packed adds of the negated
+  // threshold (FMA pipe), gathers the halves' sign bits into sign-replicated
+  // bytes (one prmt per two words) and adds the bytes with dp4a: C(t) = NE *
+  // 32 minus the negatives. h >= t iff h - t has its sign bit clear, given no
+  // image is -0 (the images are canonicalised by adding +0: -0 + 0 = +0) and a
+  // zero threshold then gives +0 - 0 = +0. The bracket is kept negated
+  // (nlo = -lo, nhi = -hi): the midpoint formula is odd-symmetric, so it
+  // yields -mid exactly.
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      s[w] = P::set_ge(h[w], m2);
-      acc = P::add(acc, s[w]);
-    }
-    u = acc * 0x10001u - P::kFold;  // (c_hi + c_lo) << 16 | c_lo
-    return warp_sum(u);
+  for (int w = 0; w < W; ++w) h[w] = P::add(h[w], 0u);
+  uint32_t nlo2 = lo2 ^ 0x80008000u, nhi2 = hi2 ^ 0x80008000u;
+  const int kneg = k - 32 * NE;  // C >= k  iff  -(negatives) >= k - M
+  auto pass = [&](uint32_t nm2, uint32_t (&s)[W], int& u) {
+#pragma unroll
+    for (int w = 0; w < W; ++w) s[w] = P::add(h[w], nm2);
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w + 1 < W; w += 2) acc = sum_bytes(half_signs(s[w], s[w + 1]), acc);
+    u = acc;  // -(this lane's negatives)
+    return int(warp_sum(uint32_t(acc)));
   };
-  // Two passes per collapse test: the midpoint always lies in [lo, hi] (as a
-  // value), so no 16-bit value strictly inside means it equals lo or hi; after
-  // a collapse the second pass counts at lo or hi, leaves the bracket as it
-  // is, and the next test ends the search. A midpoint of the other signed zero
-  // than lo / hi passes the test and costs one pass at the same value. Every
-  // pass keeps its own compares and, on C == k, writes the row from them where
-  // it ends (one exit per pass: a single shared exit measured slower).
+  // Two passes per collapse test: the midpoint always lies in the bracket (as a
+  // value), so no 16-bit value strictly inside means it equals an end; after a
+  // collapse the second pass counts at an end, leaves the bracket as it is,
+  // and the next test ends the search (a midpoint of the other signed zero
+  // than an end passes the test and costs one pass at the same value). Every
+  // pass keeps its own differences and, on C == k, writes the row from them
+  // where it ends (one exit per pass: a single shared exit measured slower).
   // Measured on GB300 (2^20 x 256 fp32, k = 32) and not kept: a test every 3
-  // or 4 passes, a pairwise-sum tree, bracket updates as integer multiply-adds
-  // (off the ALU pipe), a bracket top from the warp maximum instead of max |x|,
-  // and a row loop unrolled over the ring stages -- each 1-20% slower.
+  // or 4 passes, 1.0 / 0.0 compares (set.ge, ALU pipe) summed with fp16 adds
+  // (323.5 against 320.9 us; bf16 359.2 against 349.8), the same compares
+  // summed with integer adds + dp2a (358), bracket updates as integer
+  // multiply-adds, a bracket top from the warp maximum instead of max |x|, and
+  // a row loop unrolled over the ring stages -- each 1-20% slower.
   for (;;) {
-    uint32_t m2 = P::midpoint(lo2, hi2);
-    if (m2 == lo2 || m2 == hi2) break;
+    uint32_t nm2 = P::midpoint(nlo2, nhi2);
+    if (nm2 == nlo2 || nm2 == nhi2) break;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      if (j > 0) m2 = P::midpoint(lo2, hi2);
-      uint32_t s[W], u;
-      const uint32_t tot = pass(m2, s, u);
-      const bool ge = tot >= k0;
-      if (ge && tot < k1) {
+      if (j > 0) nm2 = P::midpoint(nlo2, nhi2);
+      uint32_t s[W];
+      int u;
+      const int tot = pass(nm2, s, u);
+      const bool ge = tot >= kneg;
+      if (tot == kneg) {
         // C(mid) == k: {h >= mid} is the top-k
-        stage_exact<W>(s, u >> 16, lane, list_addr);
+        stage_exact<W, true>(s, uint32_t(NE + u), lane, list_addr);
         copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
         return;
       }
-      lo2 = ge ? m2 : lo2;
-      hi2 = ge ? hi2 : m2;
+      nlo2 = ge ? nm2 : nlo2;
+      nhi2 = ge ? nhi2 : nm2;
     }
   }
+  lo2 = nlo2 ^ 0x80008000u;
+  hi2 = nhi2 ^ 0x80008000u;
 
   // ---- collapsed: the rest of the top-k lies in the bucket {lo <= h < hi}
   float x[NE];
@@ -613,43 +655,57 @@ __device__ __forceinline__ void process_row_bucketed(const uint32_t* __restrict_
   const float lo_b = seg_min_nan<LB>(kb <= LB ? mx : mn);
   uint32_t lo2 = P::splat(lo_b);
   uint32_t hi2 = next_up16(P::splat(top));
+  // Counting as in process_row: h - t per half with packed adds of the
+  // negated threshold, the negative halves summed as bytes (images
+  // canonicalised so that no image is -0); the brackets are kept negated.
+#pragma unroll
+  for (int w = 0; w < W; ++w) h[w] = P::add(h[w], 0u);
+  uint32_t nlo2 = lo2 ^ 0x80008000u, nhi2 = hi2 ^ 0x80008000u;
+  auto lane_count = [&](uint32_t nt2, uint32_t (&d)[W]) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) d[w] = P::add(h[w], nt2);
+#pragma unroll
+    for (int w = 0; w + 1 < W; w += 2) acc = sum_bytes(half_signs(d[w], d[w + 1]), acc);
+    return uint32_t(NE + acc);
+  };
   // Branch-free per bucket: once no 16-bit value lies strictly inside the
-  // bracket (the midpoint equals lo or hi), the pass counts at lo; if C == k / B
-  // there the bucket's threshold is found (this catches a starting lower end
-  // that already holds exactly k / B elements), else the bucket is done
-  // unresolved (tied images at its k/B-th value). A finished bucket keeps its
-  // bracket (lo = its threshold when found).
+  // bracket (the midpoint equals an end), the pass counts at the lower end; if
+  // C == k / B there the bucket's threshold is found (this catches a starting
+  // lower end that already holds exactly k / B elements), else the bucket is
+  // done unresolved (tied images at its k/B-th value). A finished bucket keeps
+  // its bracket (lower end = its threshold when found).
   bool done = false, exact = false;
   for (;;) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const uint32_t mid = P::midpoint(lo2, hi2);
-      const bool coll = mid == lo2 || mid == hi2;
-      const uint32_t m2 = coll ? lo2 : mid;
-      uint32_t acc = P::kMagic2;
-#pragma unroll
-      for (int w = 0; w < W; ++w) acc = P::add(acc, P::set_ge(h[w], m2));
-      const int cb = int(bucket_sum<B>((acc * 0x10001u - P::kFold) >> 16, b));
+      const uint32_t nmid = P::midpoint(nlo2, nhi2);
+      const bool coll = nmid == nlo2 || nmid == nhi2;
+      const uint32_t nm2 = coll ? nlo2 : nmid;
+      uint32_t d[W];
+      const int cb = int(bucket_sum<B>(lane_count(nm2, d), b));
       const bool hit = cb == kb, ge = cb >= kb;
-      lo2 = (!done && ge) ? m2 : lo2;
-      hi2 = (!done && !ge) ? m2 : hi2;
+      nlo2 = (!done && ge) ? nm2 : nlo2;
+      nhi2 = (!done && !ge) ? nm2 : nhi2;
       exact = exact || (!done && hit);
       done = done || hit || coll;
     }
     if (__all_sync(FULL, done)) break;
   }
+  lo2 = nlo2 ^ 0x80008000u;
+  hi2 = nhi2 ^ 0x80008000u;
   // Buckets with a threshold: their kept sets {h >= lo} placed in one pass.
   // An unresolved bucket reserves its k / B list positions (its first lane
-  // counts k / B, its lanes store nothing) and is finished below.
+  // counts k / B, its lanes store nothing: all differences negative) and is
+  // finished below.
   uint32_t sw[W];
-  uint32_t acc = P::kMagic2;
+  const uint32_t cex = lane_count(nlo2, sw);
+  if (!exact) {
 #pragma unroll
-  for (int w = 0; w < W; ++w) {
-    sw[w] = exact ? P::set_ge(h[w], lo2) : 0u;
-    acc = P::add(acc, sw[w]);
+    for (int w = 0; w < W; ++w) sw[w] = 0x80008000u;
   }
-  const uint32_t cl = exact ? (acc * 0x10001u - P::kFold) >> 16 : ((lane % LB) == 0 ? uint32_t(kb) : 0u);
-  stage_exact<W>(sw, cl, lane, static_cast<uint32_t>(__cvta_generic_to_shared(list)));
+  const uint32_t cl = exact ? cex : ((lane % LB) == 0 ? uint32_t(kb) : 0u);
+  stage_exact<W, true>(sw, cl, lane, static_cast<uint32_t>(__cvta_generic_to_shared(list)));
   const unsigned open = __ballot_sync(FULL, !exact);
   if (open != 0u) {
     // unresolved buckets (tied images at the k/B-th value): exact binary32

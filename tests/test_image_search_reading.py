@@ -120,3 +120,24 @@ def test_bucket_finish_is_needed():
         wrong += not np.array_equal(np.sort(np.concatenate([keep, fill])), want[r])
         assert np.array_equal(_image_search(x[r], 32, False), want[r])
     assert wrong > 0
+
+
+def test_sign_of_the_rounded_difference_decides_the_compare():
+    """The 16-bit search counts h >= t as "RN(h - t) has its sign bit clear".
+    That holds for every finite binary16 image h other than -0 (images are
+    canonicalised by adding +0) and every threshold t, zeros and subnormals
+    included: checked exhaustively over all finite images against thresholds
+    spread over the whole range (numpy's binary16 subtraction rounds once, to
+    nearest even)."""
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    h = h[np.isfinite(h)]
+    h = h[h.view(np.uint16) != 0x8000]          # canonical: no -0
+    rng = np.random.default_rng(0)
+    special = np.array([0.0, -0.0, 6e-8, -6e-8, 6.1e-5, -6.1e-5, 1.0, -1.0, 65504.0, -65504.0],
+                       dtype=np.float16)
+    t = np.concatenate([special, rng.choice(h, size=1500, replace=False)])
+    with np.errstate(over="ignore", invalid="ignore"):
+        for chunk in np.array_split(t, 10):
+            d = h[None, :] - chunk[:, None]
+            sign_clear = (d.view(np.uint16) & 0x8000) == 0
+            assert np.array_equal(sign_clear, h[None, :] >= chunk[:, None])
