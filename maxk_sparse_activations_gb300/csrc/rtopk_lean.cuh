@@ -469,7 +469,9 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
 
   // ---- coarse bisection on 16-bit images: C(lo2) >= k > C(hi2) = 0
   uint32_t lo2 = P::splat(lo_src);
-  uint32_t hi2 = next_up16(P::splat(hi32));
+  // fp32: hi32 = max |x| >= 0, whose image is +0 or positive: the next 16-bit
+  // value is one bit pattern up
+  uint32_t hi2 = sizeof(T) == 4 ? P::splat(hi32) + 0x00010001u : next_up16(P::splat(hi32));
   const uint32_t list_addr = static_cast<uint32_t>(__cvta_generic_to_shared(list));
   // A pass forms d = h - t per half with packed adds of the negated
   // threshold (FMA pipe), gathers the halves' sign bits into sign-replicated

@@ -433,3 +433,29 @@ def test_bucketed_exact_side_by_side_buckets(value_set, dtype, M):
             torch.cuda.synchronize()
             ov, oi = oracle.bucketed_topk(x, k, B)
             assert_same_selection(v, i, ov, oi, what=f"bucketed {value_set} {dtype} M={M} B={B} k={k}")
+
+
+@pytest.mark.parametrize("M", [2048, 4096, 8192])
+@pytest.mark.parametrize("value_set", ["normal", "int_ties", "dense_bucket", "signed_zeros", "wide_range"])
+def test_long_rows_default_path_bf16_and_maxk_forward(M, value_set):
+    """Exact rows of 2048 / 4096 / 8192 without pass counts (a team of 2 / 4 /
+    8 warps per row, 16-bit images): bf16 through rtopk_select (int32
+    indices) and maxk_forward (int16 indices), every row against the oracle,
+    k up to 1024; 301 rows leave a ragged last block of teams."""
+    N = 301
+    xb = synth.make(value_set, N, M, seed=M + 11, dtype="bf16")
+    xt = to_dev(xb)
+    for k in (1, 33, 64, 256, 1024):
+        ov, oi, _ = oracle_rows(oracle.replay, xb, k)
+        v, i = api.rtopk_select(xt, k)
+        fv, fi = api.maxk_forward(xt, k)
+        torch.cuda.synchronize()
+        assert_same_selection(v, i, ov, oi, what=f"bf16 M={M} {value_set} k={k}")
+        assert_same_selection(fv, fi, ov, oi, what=f"maxk_forward M={M} {value_set} k={k}")
+    xf = synth.make(value_set, N, M, seed=M + 12)
+    xft = to_dev(xf)
+    for k in (1, 33, 64, 256, 1024):
+        ov, oi, _ = oracle_rows(oracle.replay, xf, k)
+        v, i = api.rtopk_select(xft, k)
+        torch.cuda.synchronize()
+        assert_same_selection(v, i, ov, oi, what=f"f32 M={M} {value_set} k={k}")
