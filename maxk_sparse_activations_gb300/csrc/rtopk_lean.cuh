@@ -376,28 +376,37 @@ __device__ __forceinline__ void copy_out(const uint32_t* __restrict__ list, cons
 
 // Exact binary32 search from a valid bracket [lo, hi] (c(lo) >= k > c(hi)),
 // then the general fill. Used inside the last 16-bit bucket (and for the
-// rare bf16 bracket that ends on two non-adjacent values).
+// rare bf16 bracket that ends on two non-adjacent values). The bracket is
+// bisected on order-preserving integer keys of binary32 (f2o), not on value
+// midpoints: exact mode selects one set whatever thresholds are visited, and
+// a key bisection ends within 32 passes for any range, where a value
+// bisection from a small value up to a 1e30 outlier (whose 16-bit image
+// saturates, so the 16-bit bracket collapses at once) takes 100+ passes.
+// The count at a key is the count at its value, so -0 and +0 count alike;
+// a final bracket [-0, +0) cannot occur (c(-0) == c(+0)).
 template <int NE>
 __device__ __forceinline__ void finish_binary32(const float (&x)[NE], float lo, float hi, int k, int lane,
                                                 uint32_t* __restrict__ list, uint32_t& st, bool active = true,
                                                 int base = 0) {
-  int it = 0;
-  for (;; ++it) {
-    const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
-    if (!(lo < mid && mid < hi)) break;
+  int olo = f2o(lo), ohi = f2o(hi);
+  for (int it = 0;; ++it) {
+    const uint32_t gap = uint32_t(ohi) - uint32_t(olo);
+    if (gap < 2u) break;  // adjacent keys: nothing strictly inside
     if (it >= kSafetyCap) {
       st |= kStatusSafetyCap;
       break;
     }
+    const int om = olo + int(gap >> 1);
+    const float mid = o2f(om);
     uint32_t c = 0;
 #pragma unroll
     for (int e = 0; e < NE; ++e) c += (active && x[e] >= mid) ? 1u : 0u;
     const int cnt = int(warp_sum(c));
-    if (cnt >= k) lo = mid;
-    else hi = mid;
+    if (cnt >= k) olo = om;
+    else ohi = om;
     if (cnt == k) break;
   }
-  stage_general<NE>(x, lo, hi, k, lane, list, active, base);
+  stage_general<NE>(x, o2f(olo), o2f(ohi), k, lane, list, active, base);
 }
 
 // ---- one row ------------------------------------------------------------------

@@ -323,24 +323,27 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
     }
     float dummy = pos_inf();
     block_max_min_min<TW>(bmax, bmin, dummy, xc, par, lane, wib, bid);
-    float flo = bmin;
-    float fhi = next_up_f32(bmax);
-    int it = 0;
-    for (;; ++it) {
-      const float mid = __fmul_rn(__fadd_rn(flo, fhi), 0.5f);
-      if (!(flo < mid && mid < fhi)) break;
+    // exact binary32 search on order-preserving keys (as the warp kernel's
+    // finish: at most 32 passes for any range, e.g. up to 1e30 outliers)
+    int olo = f2o(bmin), ohi = f2o(next_up_f32(bmax));
+    for (int it = 0;; ++it) {
+      const uint32_t gap = uint32_t(ohi) - uint32_t(olo);
+      if (gap < 2u) break;
       if (it >= kSafetyCap) {
         st |= kStatusSafetyCap;
         break;
       }
+      const int om = olo + int(gap >> 1);
+      const float mid = o2f(om);
       int c = 0;
 #pragma unroll
       for (int e = 0; e < NE; ++e) c += (x[e] >= mid) ? 1 : 0;
       const int cnt = block_sum<TW>(c, xc, par, lane, wib, bid);
-      if (cnt >= k) flo = mid;
-      else fhi = mid;
+      if (cnt >= k) olo = om;
+      else ohi = om;
       if (cnt == k) break;
     }
+    const float flo = o2f(olo), fhi = o2f(ohi);
     stage_general_block<NE, TW>(x, flo, fhi, k, t, list, xc, par, lane, wib, bid);
   }
   team_sync<TW>(bid);
