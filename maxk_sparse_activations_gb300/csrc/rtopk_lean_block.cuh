@@ -266,8 +266,43 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
   // ---- coarse bisection on 16-bit images (sign-bit counts, negated bracket)
 #pragma unroll
   for (int w = 0; w < W; ++w) h[w] = P::add(h[w], 0u);  // no image is -0
-  const uint32_t lo2 = P::splat(lo_src);
-  const uint32_t hi2 = sizeof(T) == 4 ? P::splat(hi32) + 0x00010001u : next_up16(P::splat(hi32));
+  uint32_t lo2 = P::splat(lo_src);
+  uint32_t hi2 = sizeof(T) == 4 ? P::splat(hi32) + 0x00010001u : next_up16(P::splat(hi32));
+  if constexpr (sizeof(T) == 4) {
+    if (hi2 == 0x7c007c00u) {
+      // max |x| saturates the binary16 image (|x| >= 65488): a bracket up to
+      // +inf would collapse at its first midpoint. Count the images at +65504
+      // and -65504 and take the extremes of the others (one exchange each),
+      // then start from a bracket that still has C(lo) >= k > C(hi):
+      //   C(65504) >= k: [65504, +inf), the binary32 finish over those;
+      //   else hi = the 16-bit value above the largest other image (or 65504),
+      //   and for k > TT lo = the smallest other image when at least k images
+      //   lie above -65504 (else -65504, where C = M).
+      int sat = 0;
+      float mxn = neg_inf(), mnn = pos_inf();
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float hv = half ? P::high_f32(h[w]) : P::low_f32(h[w]);
+          const bool ps = hv == 65504.0f, ns = hv == -65504.0f;
+          sat += (ps ? 1 : 0) + (ns ? 0x10000 : 0);
+          mxn = (ps || ns) ? mxn : fmaxf(mxn, hv);
+          mnn = (ps || ns) ? mnn : fminf(mnn, hv);
+        }
+      }
+      const int both = block_sum<TW>(sat, xc, par, lane, wib, bid);
+      float unused = pos_inf();
+      block_max_min_min<TW>(mxn, mnn, unused, xc, par, lane, wib, bid);
+      const int npos = both & 0xffff, nneg = both >> 16;
+      if (npos >= k) {
+        lo2 = 0x7bff7bffu;
+      } else {
+        hi2 = mxn == neg_inf() ? 0x7bff7bffu : next_up16(P::splat(mxn));
+        if (k > TT) lo2 = (TT * NE - nneg >= k && mnn != pos_inf()) ? P::splat(mnn) : 0xfbfffbffu;
+      }
+    }
+  }
   uint32_t nlo2 = lo2 ^ 0x80008000u, nhi2 = hi2 ^ 0x80008000u;
   const int kneg = k - TT * NE;  // C >= k  iff  -(negatives) >= k - M
   for (;;) {

@@ -459,3 +459,40 @@ def test_long_rows_default_path_bf16_and_maxk_forward(M, value_set):
         v, i = api.rtopk_select(xft, k)
         torch.cuda.synchronize()
         assert_same_selection(v, i, ov, oi, what=f"f32 M={M} {value_set} k={k}")
+
+
+def _saturating_rows(case, N, M, seed):
+    """fp32 rows whose binary16 images saturate at +-65504 in bulk: half of the
+    entries +-1e30; 90% at -1e30 with 2% at +1e30; or values around the
+    binary16 rounding boundary (65488 rounds to 65472, above it to 65504)."""
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((N, M)).astype(np.float32)
+    u = g.random((N, M))
+    if case == "half_outliers":
+        x = np.where(u < 0.25, np.float32(1e30), np.where(u < 0.5, np.float32(-1e30), x))
+    elif case == "mostly_negative":
+        x = np.where(u < 0.9, np.float32(-1e30), np.where(u < 0.92, np.float32(1e30), x))
+    else:
+        pool = np.array([65472.0, 65487.99, 65488.0, 65488.01, 65504.0, 65520.0, 1e30], dtype=np.float32)
+        pick = pool[g.integers(0, pool.size, size=(N, M))]
+        sign = np.where(g.random((N, M)) < 0.5, np.float32(-1), np.float32(1))
+        x = np.where(u < 0.6, pick * sign, x * np.float32(1000))
+    return np.ascontiguousarray(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("case", ["half_outliers", "mostly_negative", "boundary"])
+@pytest.mark.parametrize("M", [2048, 4096, 8192])
+def test_long_rows_saturated_images(M, case):
+    """Exact rows of 2048 / 4096 / 8192 whose 16-bit images saturate in bulk:
+    the bracket starts from the counts at +-65504 and the extremes of the other
+    images (all three branches: C(65504) >= k, a lower end above -65504, and
+    -65504 itself), every row against the definition, k on both sides of the
+    team's thread count."""
+    N = 97
+    x = _saturating_rows(case, N, M, seed=M + len(case))
+    xt = to_dev(x)
+    for k in (1, 64, 200, 1024):
+        v, i = api.rtopk_select(xt, k)
+        torch.cuda.synchronize()
+        ov, oi = oracle.sort_topk(x, k)
+        assert_same_selection(v, i, ov, oi, what=f"saturated {case} M={M} k={k}")
