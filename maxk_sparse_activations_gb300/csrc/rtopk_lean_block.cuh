@@ -37,6 +37,7 @@ namespace lean {
 constexpr int kBlockListK = 1024;  // largest k of the block kernel
 
 
+
 // Shared exchange area of one team (the TW warps of a row): two alternating
 // slot sets.
 struct BlockXchg {
@@ -199,7 +200,8 @@ __device__ __forceinline__ void stage_general_block(const float (&x)[NE], float 
 template <typename T, int NE, int TW, typename IdxT>
 __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ srow, int k, int t, int lane, int wib,
                                                   int bid, uint32_t* __restrict__ list, BlockXchg& xc, int& par,
-                                                  T* __restrict__ vrow, IdxT* __restrict__ irow, uint32_t& st) {
+                                                  float& tprev, float& rho, T* __restrict__ vrow,
+                                                  IdxT* __restrict__ irow, uint32_t& st) {
   constexpr int TT = TW * 32;  // threads of the team
   using P = Packed16<T>;
   using I = Img<T>;
@@ -305,9 +307,38 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
   }
   uint32_t nlo2 = lo2 ^ 0x80008000u, nhi2 = hi2 ^ 0x80008000u;
   const int kneg = k - TT * NE;  // C >= k  iff  -(negatives) >= k - M
-  for (;;) {
-    const uint32_t nm2 = P::midpoint(nlo2, nhi2);
-    if (nm2 == nlo2 || nm2 == nhi2) break;  // no 16-bit value strictly inside
+  // Probes: the team's previous threshold first, then Newton steps
+  // t + (C(t) - k - 1/2) / rho with the density rho (elements per unit value
+  // near the threshold) estimated on earlier rows; a probe that is not
+  // strictly inside the bracket (as a 16-bit value) is replaced by the
+  // midpoint. Exact mode selects one set whatever thresholds are visited, so
+  // the guesses change the pass count only (CPU emulation, 2^11 .. 2^13
+  // columns, k = 64 .. 1024: 8-12.5 passes -> 4-5; GB300, 2^16 fp32 rows:
+  // M = 2048 k = 256 227 -> 182 us, M = 4096 k = 1024 496 -> 400 us, M = 8192
+  // k = 64 797 -> 717 us; bf16 rows, which often end tied, gain up to 18%
+  // at k = 1024 and lose 4% at M = 2048, k = 64). At most kGuesses probes
+  // of a row are guesses, so a poor density estimate (steps of one 16-bit
+  // value) costs at most that many extra passes. tprev, rho and
+  // every quantity below derive from team-wide sums, so all threads of the
+  // team take the same branches.
+  float lo_f = P::low_f32(lo2), hi_f = P::low_f32(hi2);
+  const float inv_rho = rho > 0.0f ? 1.0f / rho : 0.0f;
+  float t_last = tprev, t_first = 0.0f;
+  int c_last = 0, c_first = 0;  // C - k at the last / first probe
+  bool first = true;
+  constexpr int kGuesses = 8;
+  for (int pass = 0;; ++pass) {
+    // guess: the previous row's threshold (NaN when none), then Newton
+    const float tg = first ? tprev : fmaf(float(c_last) - 0.5f, inv_rho, t_last);
+    const uint32_t ng2 = P::splat(-tg);  // negated image of the guess
+    const float gv = -P::low_f32(ng2);
+    uint32_t nm2;
+    if (pass < kGuesses && lo_f < gv && gv < hi_f) {
+      nm2 = ng2;
+    } else {
+      nm2 = P::midpoint(nlo2, nhi2);
+      if (nm2 == nlo2 || nm2 == nhi2) break;  // no 16-bit value strictly inside
+    }
     uint32_t d[W];
     int acc = 0;
 #pragma unroll
@@ -315,8 +346,14 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
 #pragma unroll
     for (int w = 0; w + 1 < W; w += 2) acc = sum_bytes(half_signs(d[w], d[w + 1]), acc);
     const int tot = block_sum<TW>(acc, xc, par, lane, wib, bid);
+    const float mv = -P::low_f32(nm2);  // the probe's value
     if (tot == kneg) {
       // C(mid) == k: {h >= mid} is the top-k; this thread keeps NE + acc
+      if (!first && c_first != 0 && t_first != mv) {
+        const float est = fabsf(float(c_first)) / fabsf(t_first - mv);
+        rho = rho > 0.0f ? 0.8f * rho + 0.2f * est : est;
+      }
+      tprev = mv;
       uint32_t all;
       const uint32_t ex = block_excl_scan<TW>(uint32_t(NE + acc), all, xc, par, lane, wib, bid);
       int pos = int(ex);
@@ -332,7 +369,17 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
     const bool ge = tot >= kneg;
     nlo2 = ge ? nm2 : nlo2;
     nhi2 = ge ? nhi2 : nm2;
+    lo_f = ge ? mv : lo_f;
+    hi_f = ge ? hi_f : mv;
+    c_last = tot - kneg;
+    t_last = mv;
+    if (first) {
+      c_first = c_last;
+      t_first = mv;
+      first = false;
+    }
   }
+  tprev = lo_f;  // collapsed: the threshold lies in [lo, hi)
 
   // ---- collapsed: the rest of the top-k lies in the bucket {lo <= h < hi}
   float x[NE];
@@ -388,16 +435,14 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
 // A row of M = TW * 32 * NE elements on a team of TW warps; a block of 256
 // threads holds 8 / TW teams (rows in flight), each with its own two stages,
 // list and exchange slots. Resident blocks per SM (registers; at most about
-// 70 KB of shared memory per block): 5 at 8 elements per thread, 3 at 16; at
-// 32, 2 (128 registers, no spills) except fp32 rows of 8192 on one 8-warp team,
-// which ran faster at 3 (GB300, 2^16 rows: M = 2048 fp32 k = 64 268 -> 191 us
-// and M = 4096 k = 256 636 -> 477 us at 2; M = 8192 fp32 k = 256 939 -> 914 us
-// at 3, bf16 829 -> 800 us at 2).
+// 70 KB of shared memory per block): 5 at 8 elements per thread, 3 at 16, 2 at
+// 32 (up to 128 registers, no spills; GB300, 2^16 rows: M = 2048 fp32 k = 64
+// 268 -> 191 us against 3 blocks, M = 8192 fp32 k = 256 1184 -> 955 us).
 template <typename T, int NE, int TW>
 struct LeanBlockCfg {
   static constexpr int RW = Lane<T, NE>::RW;
   static constexpr int kTeams = 8 / TW;
-  static constexpr int kBlocks = NE <= 8 ? 5 : (NE < 32 ? 3 : ((TW == 8 && sizeof(T) == 4) ? 3 : 2));
+  static constexpr int kBlocks = NE <= 8 ? 5 : (NE < 32 ? 3 : 2);
   static constexpr size_t kTeamWords = size_t(2) * TW * 32 * RW + kBlockListK + sizeof(BlockXchg) / 4;
   static constexpr size_t kSmem = kTeams * kTeamWords * 4;
 };
@@ -430,6 +475,7 @@ rtopk_lean_block_kernel(const T* __restrict__ in, int64_t N, int k, T* __restric
   const int64_t src_step = nt * kRowWords;
   int par = 0;
   uint32_t st = 0;
+  float tprev = __int_as_float(0x7fc00000), rho = 0.0f;  // search guesses carried across the team's rows
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     issue_row_block<RW, TT>(ring_base + uint32_t(q * kRowWords * 4), src, t, q < nrows);
@@ -442,7 +488,8 @@ rtopk_lean_block_kernel(const T* __restrict__ in, int64_t N, int k, T* __restric
   for (int i = 0; i < nrows; ++i) {
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     team_sync<TW>(bid);  // every team thread's copies of this row are visible
-    process_row_block<T, NE, TW, IdxT>(ring + q * kRowWords, k, t, lane, wib, bid, list, xc, par, vrow, irow, st);
+    process_row_block<T, NE, TW, IdxT>(ring + q * kRowWords, k, t, lane, wib, bid, list, xc, par, tprev, rho, vrow,
+                                       irow, st);
     team_sync<TW>(bid);  // every team thread is done with this stage and the list
     issue_row_block<RW, TT>(ring_base + uint32_t(q * kRowWords * 4), src, t, i + 2 < nrows);
     src += src_step;
