@@ -21,6 +21,9 @@ template <typename T, int NE, typename IdxT>
 cudaError_t launch_lean(const SelectArgs& a, cudaStream_t s) {
   constexpr int kThreads = 256;
   auto kern = lean::rtopk_lean_kernel<T, NE, IdxT>;
+  if constexpr (lean::kGuessRows<T, NE>) {
+    if (a.k > 32) kern = lean::rtopk_lean_kernel<T, NE, IdxT, 1, true>;
+  }
   const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), kThreads, 0, (a.N + 7) / 8);
   if (blocks <= 0) return cudaErrorInvalidConfiguration;
   kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.k, static_cast<T*>(a.vals),

@@ -410,10 +410,10 @@ __device__ __forceinline__ void finish_binary32(const float (&x)[NE], float lo, 
 }
 
 // ---- one row ------------------------------------------------------------------
-template <typename T, int NE, typename IdxT>
+template <typename T, int NE, typename IdxT, bool GUESS>
 __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, int k, int lane,
                                             uint32_t* __restrict__ list, T* __restrict__ vrow,
-                                            IdxT* __restrict__ irow, uint32_t& st) {
+                                            IdxT* __restrict__ irow, uint32_t& st, float& tprev, float& rho) {
   using P = Packed16<T>;
   using I = Img<T>;
   constexpr int RW = Lane<T, NE>::RW;
@@ -516,24 +516,77 @@ __device__ __forceinline__ void process_row(const uint32_t* __restrict__ srow, i
   // summed with integer adds + dp2a (358), bracket updates as integer
   // multiply-adds, a bracket top from the warp maximum instead of max |x|, and
   // a row loop unrolled over the ring stages -- each 1-20% slower.
-  for (;;) {
-    uint32_t nm2 = P::midpoint(nlo2, nhi2);
-    if (nm2 == nlo2 || nm2 == nhi2) break;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j > 0) nm2 = P::midpoint(nlo2, nhi2);
-      uint32_t s[W];
+  // GUESS (the launcher's choice, kGuessRows): guessed probes, for rows where
+  // a pass is large and the bracket starts wide (k > 32: from -max |x|): the
+  // warp's previous threshold first, then Newton steps t + (C(t) - k - 1/2) /
+  // rho with the density rho estimated on the warp's earlier rows, at most
+  // kGuesses a row; a guess that is not strictly inside the bracket (as a
+  // 16-bit value) is replaced by the midpoint. Exact mode selects one set
+  // whatever thresholds are visited.
+  if constexpr (GUESS) {
+    float lo_f = P::low_f32(lo2), hi_f = P::low_f32(hi2);
+    const float inv_rho = rho > 0.0f ? 1.0f / rho : 0.0f;
+    float t_last = tprev, t_first = 0.0f;
+    int c_last = 0, c_first = 0;  // C - k at the last / first probe
+    constexpr int kGuesses = 8;
+    for (int p = 0;; ++p) {
+      const float tg = p == 0 ? tprev : fmaf(float(c_last) - 0.5f, inv_rho, t_last);
+      const uint32_t ng2 = P::splat(-tg);  // negated image of the guess
+      const float gv = -P::low_f32(ng2);
+      uint32_t nm2;
+      if (p < kGuesses && lo_f < gv && gv < hi_f) {
+        nm2 = ng2;
+      } else {
+        nm2 = P::midpoint(nlo2, nhi2);
+        if (nm2 == nlo2 || nm2 == nhi2) break;
+      }
+      uint32_t sd[W];
       int u;
-      const int tot = pass(nm2, s, u);
-      const bool ge = tot >= kneg;
+      const int tot = pass(nm2, sd, u);
+      const float mv = -P::low_f32(nm2);
       if (tot == kneg) {
-        // C(mid) == k: {h >= mid} is the top-k
-        stage_exact<W, true>(s, uint32_t(NE + u), lane, list_addr);
+        if (p > 0 && c_first != 0 && t_first != mv) {
+          const float est = fabsf(float(c_first)) / fabsf(t_first - mv);
+          rho = rho > 0.0f ? 0.8f * rho + 0.2f * est : est;
+        }
+        tprev = mv;
+        stage_exact<W, true>(sd, uint32_t(NE + u), lane, list_addr);
         copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
         return;
       }
+      const bool ge = tot >= kneg;
       nlo2 = ge ? nm2 : nlo2;
       nhi2 = ge ? nhi2 : nm2;
+      lo_f = ge ? mv : lo_f;
+      hi_f = ge ? hi_f : mv;
+      c_last = tot - kneg;
+      t_last = mv;
+      if (p == 0) {
+        c_first = c_last;
+        t_first = mv;
+      }
+    }
+    tprev = lo_f;  // collapsed: the threshold lies in [lo, hi)
+  } else {
+    for (;;) {
+      uint32_t nm2 = P::midpoint(nlo2, nhi2);
+      if (nm2 == nlo2 || nm2 == nhi2) break;
+  #pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (j > 0) nm2 = P::midpoint(nlo2, nhi2);
+        uint32_t s[W];
+        int u;
+        const int tot = pass(nm2, s, u);
+        const bool ge = tot >= kneg;
+        if (tot == kneg) {
+          // C(mid) == k: {h >= mid} is the top-k
+          stage_exact<W, true>(s, uint32_t(NE + u), lane, list_addr);
+          copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
+          return;
+        }
+        nlo2 = ge ? nm2 : nlo2;
+        nhi2 = ge ? nhi2 : nm2;
+      }
     }
   }
   lo2 = nlo2 ^ 0x80008000u;
@@ -768,7 +821,15 @@ struct LeanCfg {
 // (B > 1: B buckets per row, B dividing 32 and k). One warp per row,
 // persistent over rows; each warp keeps kStages rows in flight through
 // cp.async copies into its own shared stages.
-template <typename T, int NE, typename IdxT, int B = 1>
+// Whether rows of 32 * NE elements take guessed probes (process_row, GUESS)
+// when k > 32. Measured on GB300, 2^18 N(0,1) rows, k = 64..256: fp32 rows of
+// 1024 4-8% faster (k = 256 327 -> 303 us), bf16 rows of 512 / 1024 2-15%
+// faster; fp32 rows of 512 were not faster, and every k <= 32 (bracket from
+// the smallest lane maximum) was slower with guesses.
+template <typename T, int NE>
+constexpr bool kGuessRows = NE >= 32 || (NE >= 16 && sizeof(T) == 2);
+
+template <typename T, int NE, typename IdxT, int B = 1, bool GUESS = false>
 __global__ void __launch_bounds__(256, LeanCfg<T, NE>::kBlocks)
 rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ vals, IdxT* __restrict__ idx,
                   uint32_t* __restrict__ status) {
@@ -788,6 +849,7 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
   const uint32_t* src = reinterpret_cast<const uint32_t*>(in) + r0 * kRowWords + lane * 4;  // next row to issue
   const int64_t src_step = nw * kRowWords;
   uint32_t st = 0;
+  float tprev = __int_as_float(0x7fc00000), rho = 0.0f;  // search guesses carried across the warp's rows
   // prologue: the warp's first S rows
 #pragma unroll
   for (int q = 0; q < S; ++q) {
@@ -802,7 +864,7 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
     wait_rows<S - 1>();  // this row's copy group is complete
     __syncwarp();
     if constexpr (B == 1) {
-      process_row<T, NE, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
+      process_row<T, NE, IdxT, GUESS>(ring_all[wib][q], k, lane, list, vrow, irow, st, tprev, rho);
     } else {
       process_row_bucketed<T, NE, B, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
     }
