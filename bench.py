@@ -739,9 +739,20 @@ def _case_bucketed():
         api.rtopk_select_bucketed(x, 32, 4)
 
 
+def _case_long_rows():
+    # exact rows of 4096 (the multi-warp 16-bit kernel, four warps per row):
+    # 2^14 x 4096 fp32 N(0,1), k = 256 (268 MB in)
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    x = torch.from_numpy(synth.normal_f32(1 << 14, 4096, seed=0)).to(dev)
+    for _ in range(3):
+        api.rtopk_select(x, 256)
+
+
 PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward,
                  "maxk-forward": _case_maxk_forward, "maxk-backward": _case_maxk_backward,
-                 "bucketed": _case_bucketed}
+                 "bucketed": _case_bucketed, "long-rows": _case_long_rows}
 
 
 def run_case(name: str) -> int:
