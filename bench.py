@@ -750,7 +750,18 @@ def _case_long_rows():
         api.rtopk_select(x, 256)
 
 
-PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward,
+def _case_early_stop():
+    # early stop (max_iter = 2, the replay kernel) on a quarter of the headline
+    # matrix: 2^18 x 256 fp32 N(0,1), k = 32 (268 MB in)
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    x = torch.from_numpy(synth.normal_f32(1 << 18, 256, seed=0)).to(dev)
+    for _ in range(3):
+        api.rtopk_select(x, 32, 2)
+
+
+PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward, "early-stop": _case_early_stop,
                  "maxk-forward": _case_maxk_forward, "maxk-backward": _case_maxk_backward,
                  "bucketed": _case_bucketed, "long-rows": _case_long_rows}
 

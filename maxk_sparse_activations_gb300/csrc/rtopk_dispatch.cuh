@@ -31,6 +31,18 @@ cudaError_t launch_lean(const SelectArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Full rows of 32 * NE elements in replay mode: rtopk_lean_replay_kernel.
+template <typename T, int NE, typename IdxT>
+cudaError_t launch_lean_replay(const SelectArgs& a, cudaStream_t s) {
+  constexpr int kThreads = 256;
+  auto kern = lean::rtopk_lean_replay_kernel<T, NE, IdxT>;
+  const int blocks = persistent_blocks(reinterpret_cast<const void*>(kern), kThreads, 0, (a.N + 7) / 8);
+  if (blocks <= 0) return cudaErrorInvalidConfiguration;
+  kern<<<blocks, kThreads, 0, s>>>(static_cast<const T*>(a.in), a.N, a.k, a.max_iter, a.eps,
+                                   static_cast<T*>(a.vals), static_cast<IdxT*>(a.idx), a.iters, a.status);
+  return cudaGetLastError();
+}
+
 // One warp per row (W = 1). L = compaction list entries per lane (0 = off).
 // Measured on GB300 (2^18 N(0,1) rows): compaction costs more than it saves
 // while a lane holds few elements (M = 256: 187 vs 160 us), and pays from 32
@@ -45,6 +57,12 @@ cudaError_t launch_warp(const SelectArgs& a, bool full, bool vec, cudaStream_t s
     // exact mode without pass counts on full rows: the search counts on
     // packed 16-bit images of the row (rtopk_lean.cuh)
     if (exact && a.iters == nullptr && full && a.k <= lean::kListK) return launch_lean<T, NE, IdxT>(a, s);
+    // early stop / eps on full rows: the replay on the same row ring (GB300,
+    // 2^20 x 256 fp32, k = 32: max_iter = 2 494 -> 396 us, max_iter = 5 617 ->
+    // 505 us). Exact mode with pass counts stays on the binary32 warp kernel,
+    // whose exact-threshold exit is cheaper than the replay's general fill
+    // (589 against 626 us).
+    if (!exact && full && a.k <= lean::kListK) return launch_lean_replay<T, NE, IdxT>(a, s);
   }
   const int L = (NE >= 64 && a.k <= 128) ? 8 : ((NE >= 32 && a.k <= 64) ? 4 : 0);
   using K = void (*)(const T*, int64_t, int, int, int, float, bool, bool, T*, IdxT*, int*, uint32_t*);

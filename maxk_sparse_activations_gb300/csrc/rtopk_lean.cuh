@@ -98,6 +98,32 @@ __device__ __forceinline__ int sum_bytes(uint32_t a, int c) {
   return d;
 }
 
+// c + minus the number of set sign bits of the binary32 words a and b: prmt
+// copies their sign bits into bytes 0 and 1 as 0xff / 0x00 (bytes 2 and 3
+// get weight 0 in the dp4a).
+__device__ __forceinline__ int sum_sign_pair(uint32_t a, uint32_t b, int c) {
+  uint32_t p;
+  asm("prmt.b32 %0, %1, %2, 0x00FB;" : "=r"(p) : "r"(a), "r"(b));
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(p), "r"(0x00000101), "r"(c));
+  return d;
+}
+
+// Number of a lane's values x >= t, for canonical values (no -0) and finite
+// t: d = x - t has its sign bit clear iff x >= t (x == t gives +0, and a
+// nonzero difference of binary32 values never rounds to zero), so a pass is
+// subtractions on the FMA pipe and one prmt + one dp4a per two values instead
+// of a compare and an add per value.
+template <int NE>
+__device__ __forceinline__ uint32_t lane_count_ge(const float (&x)[NE], float t) {
+  int acc = 0;
+#pragma unroll
+  for (int e = 0; e + 1 < NE; e += 2)
+    acc = sum_sign_pair(__float_as_uint(__fsub_rn(x[e], t)), __float_as_uint(__fsub_rn(x[e + 1], t)), acc);
+  if constexpr ((NE & 1) != 0) acc -= int(__float_as_uint(__fsub_rn(x[NE - 1], t)) >> 31);
+  return uint32_t(NE + acc);
+}
+
 // NaN-propagating maximum of a lane's values.
 template <int NE>
 __device__ __forceinline__ float lane_max(const float (&x)[NE]) {
@@ -802,6 +828,83 @@ __device__ __forceinline__ void process_row_bucketed(const uint32_t* __restrict_
   copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
 }
 
+// ---- one row, replay of the value-space bisection ---------------------------
+// Early stop (max_iter cap, eps) or exact mode with per-row pass counts: the
+// RTop-K summary page, "Approach": bisection over the row's value range
+// [min, max] with the binary32 midpoint (lo + hi) * 0.5, at most `limit`
+// counting passes, stopping once hi - lo <= eps, once no binary32 value lies
+// strictly inside, or at a threshold that keeps exactly k; then every x >= hi
+// is kept and the rest of k comes from lo <= x < hi by ascending index (the
+// general fill). When ties at the row maximum alone fill k, the k
+// lowest-index maxima are kept after no pass. Every comparison, midpoint and
+// difference is binary32 and rounded as written, so the pass count and the
+// kept set are those of the plain sequential replay.
+template <typename T, int NE, typename IdxT>
+__device__ __forceinline__ void process_row_replay(const uint32_t* __restrict__ srow, int k, int limit,
+                                                   bool cap_is_safety, float eps, int lane,
+                                                   uint32_t* __restrict__ list, T* __restrict__ vrow,
+                                                   IdxT* __restrict__ irow, int* __restrict__ it_out,
+                                                   uint32_t& st) {
+  constexpr unsigned FULL = 0xffffffffu;
+  float x[NE];
+  reload<T, NE>(srow, lane, x);
+  float mx = x[0], mn = x[0];
+  int e = 1;
+#pragma unroll
+  for (; e + 1 < NE; e += 2) {
+    mx = max3_nan(mx, x[e], x[e + 1]);
+    mn = min3_nan(mn, x[e], x[e + 1]);
+  }
+  if (e < NE) {
+    mx = max_nan(mx, x[e]);
+    mn = min_nan(mn, x[e]);
+  }
+  float hi = warp_max_nan(mx), lo = warp_min_nan(mn);
+  int it = 0;
+#pragma unroll
+  for (int q = 0; q < NE; ++q) x[q] = __fadd_rn(x[q], 0.0f);  // -0 -> +0 (counts, not output bits)
+  if (!(hi <= 1e38f && lo >= -1e38f)) {
+    // invalid row: report which precondition fails, write the first k elements
+    bool nonfinite = false, range = false;
+#pragma unroll
+    for (int q = 0; q < NE; ++q) {
+      const float a = fabsf(x[q]);
+      nonfinite |= !(a <= 3.402823466e38f);
+      range |= (a > 1e38f && a <= 3.402823466e38f);
+    }
+    if (__any_sync(FULL, nonfinite)) st |= kStatusNonFinite;
+    if (__any_sync(FULL, range)) st |= kStatusRange;
+    for (int p = lane; p < k; p += 32) list[p] = uint32_t(p);
+  } else {
+    // ties at the maximum fill k only if k / NE lanes hold the maximum
+    bool max_tie = false;
+    if (__popc(__ballot_sync(FULL, mx == hi)) * NE >= k) max_tie = int(warp_sum(lane_count_ge<NE>(x, hi))) >= k;
+    if (max_tie) {
+      lo = hi;  // [max, next above max): the maxima, filled by lowest index
+      hi = next_up_f32(hi);
+    } else {
+      // invariant: c(lo) >= k > c(hi)
+      for (;;) {
+        if (it >= limit) {
+          if (cap_is_safety) st |= kStatusSafetyCap;
+          break;
+        }
+        if (!(__fsub_rn(hi, lo) > eps)) break;
+        const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
+        if (!(lo < mid && mid < hi)) break;
+        const int cnt = int(warp_sum(lane_count_ge<NE>(x, mid)));
+        ++it;
+        if (cnt >= k) lo = mid;
+        else hi = mid;
+        if (cnt == k) break;
+      }
+    }
+    stage_general<NE>(x, lo, hi, k, lane, list);
+  }
+  if (it_out != nullptr && lane == 0) *it_out = it;
+  copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
+}
+
 #ifndef RTOPK_LEAN_MIN_BLOCKS
 #define RTOPK_LEAN_MIN_BLOCKS 5
 #endif
@@ -817,10 +920,6 @@ struct LeanCfg {
       NE <= 8 ? RTOPK_LEAN_MIN_BLOCKS : ((NE >= 32 && sizeof(T) == 4) ? 2 : 3);
 };
 
-// Full rows of 32 * NE elements, exact mode, k <= kListK, 16-byte aligned
-// (B > 1: B buckets per row, B dividing 32 and k). One warp per row,
-// persistent over rows; each warp keeps kStages rows in flight through
-// cp.async copies into its own shared stages.
 // Whether rows of 32 * NE elements take guessed probes (process_row, GUESS)
 // when k > 32. Measured on GB300, 2^18 N(0,1) rows, k = 64..256: fp32 rows of
 // 1024 4-8% faster (k = 256 327 -> 303 us), bf16 rows of 512 / 1024 2-15%
@@ -829,6 +928,10 @@ struct LeanCfg {
 template <typename T, int NE>
 constexpr bool kGuessRows = NE >= 32 || (NE >= 16 && sizeof(T) == 2);
 
+// Full rows of 32 * NE elements, exact mode, k <= kListK, 16-byte aligned
+// (B > 1: B buckets per row, B dividing 32 and k). One warp per row,
+// persistent over rows; each warp keeps kStages rows in flight through
+// cp.async copies into its own shared stages.
 template <typename T, int NE, typename IdxT, int B = 1, bool GUESS = false>
 __global__ void __launch_bounds__(256, LeanCfg<T, NE>::kBlocks)
 rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ vals, IdxT* __restrict__ idx,
@@ -873,6 +976,58 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
     src += src_step;
     vrow += out_step;
     irow += out_step;
+    q = (q + 1 == S) ? 0 : q + 1;
+  }
+  wait_rows<0>();
+  if (status != nullptr && st != 0u && lane == 0) atomicOr(status, st);
+}
+
+// Full rows of 32 * NE elements, replay mode (process_row_replay: early stop,
+// eps, or pass counts written to iters when it is not null), k <= kListK,
+// 16-byte aligned; the same row ring as rtopk_lean_kernel.
+template <typename T, int NE, typename IdxT>
+__global__ void __launch_bounds__(256, LeanCfg<T, NE>::kBlocks)
+rtopk_lean_replay_kernel(const T* __restrict__ in, int64_t N, int k, int max_iter, float eps, T* __restrict__ vals,
+                         IdxT* __restrict__ idx, int* __restrict__ iters, uint32_t* __restrict__ status) {
+  constexpr int RW = Lane<T, NE>::RW;
+  constexpr int S = LeanCfg<T, NE>::kStages;
+  constexpr int kRowWords = 32 * RW;
+  __shared__ __align__(16) uint32_t ring_all[8][S][kRowWords];
+  __shared__ uint32_t list_all[8][kListK];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  uint32_t* list = list_all[wib];
+  const int64_t nw = int64_t(gridDim.x) * 8;
+  const int64_t r0 = int64_t(blockIdx.x) * 8 + wib;
+  const int nrows = r0 < N ? int((N - 1 - r0) / nw) + 1 : 0;  // rows r0, r0 + nw, ... < N
+  constexpr uint32_t kStageBytes = uint32_t(kRowWords) * 4u;
+  const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring_all[wib][0]));
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(in) + r0 * kRowWords + lane * 4;  // next row to issue
+  const int64_t src_step = nw * kRowWords;
+  const bool cap_is_safety = (max_iter < 0 || max_iter > kSafetyCap);
+  const int limit = cap_is_safety ? kSafetyCap : max_iter;
+  uint32_t st = 0;
+#pragma unroll
+  for (int q = 0; q < S; ++q) {
+    issue_row<RW>(ring_base + uint32_t(q) * kStageBytes, src, lane, q < nrows);
+    src += src_step;
+  }
+  T* vrow = vals + r0 * int64_t(k);
+  IdxT* irow = idx + r0 * int64_t(k);
+  int* itrow = iters != nullptr ? iters + r0 : nullptr;
+  const int64_t out_step = nw * int64_t(k);
+  int q = 0;
+  for (int i = 0; i < nrows; ++i) {
+    wait_rows<S - 1>();  // this row's copy group is complete
+    __syncwarp();
+    process_row_replay<T, NE, IdxT>(ring_all[wib][q], k, limit, cap_is_safety, eps, lane, list, vrow, irow, itrow,
+                                    st);
+    // copy_out ends with __syncwarp: every lane is done with this stage
+    issue_row<RW>(ring_base + uint32_t(q) * kStageBytes, src, lane, i + S < nrows);
+    src += src_step;
+    vrow += out_step;
+    irow += out_step;
+    if (itrow != nullptr) itrow += nw;
     q = (q + 1 == S) ? 0 : q + 1;
   }
   wait_rows<0>();

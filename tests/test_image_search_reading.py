@@ -141,3 +141,29 @@ def test_sign_of_the_rounded_difference_decides_the_compare():
             d = h[None, :] - chunk[:, None]
             sign_clear = (d.view(np.uint16) & 0x8000) == 0
             assert np.array_equal(sign_clear, h[None, :] >= chunk[:, None])
+
+
+def test_binary32_difference_sign_decides_the_compare():
+    """The binary32 counting pass reads x >= t off the sign bit of the rounded
+    difference x - t. For x without -0 and finite t this holds for every pair:
+    equal values give +0 (x - x rounds to +0 in round-to-nearest), and a nonzero
+    difference of binary32 values never rounds to zero with gradual underflow
+    (it is at least the smallest subnormal). Checked over zeros of both signs
+    as t, subnormals, values around the extremes, and random bit patterns."""
+    rng = np.random.default_rng(11)
+    special = np.array([0.0, -0.0, 1e-45, -1e-45, 2e-45, -2e-45, 1.1754942e-38, -1.1754942e-38,
+                        1.1754944e-38, -1.1754944e-38, 1.0, -1.0, 1e38, -1e38, 3.0e38, -3.0e38],
+                       dtype=F32)
+    bits = rng.integers(0, 1 << 32, size=4000, dtype=np.uint64).astype(np.uint32)
+    rand = bits.view(F32)
+    rand = rand[np.isfinite(rand) & (np.abs(rand) <= F32(1e38))]
+    subn = (rng.integers(1, 1 << 23, size=500, dtype=np.uint32)
+            | (rng.integers(0, 2, size=500, dtype=np.uint32) << np.uint32(31))).view(F32)
+    vals = np.concatenate([special, rand, subn]).astype(F32)
+    x = vals + F32(0.0)  # canonical: -0 -> +0
+    assert not np.any((x == 0) & np.signbit(x))
+    with np.errstate(over="ignore"):
+        for t in vals:
+            d = (x - t).astype(F32)
+            got = ~np.signbit(d)
+            np.testing.assert_array_equal(got, x >= t, err_msg=f"t={t!r}")
