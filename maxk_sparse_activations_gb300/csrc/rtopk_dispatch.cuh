@@ -119,9 +119,11 @@ cudaError_t launch_short_rows(const SelectArgs& a, cudaStream_t s) {
   const int M = a.M;
   const bool vec = (M % V == 0) && aligned16(a.in);
   if constexpr (sizeof(T) == 2) {
-    // bf16 rows of 128 (4 per lane, 8 bytes): the lean kernel in exact mode
-    if (M == 128 && vec && a.max_iter < 0 && a.eps == 0.0f && a.iters == nullptr && a.k <= lean::kListK)
-      return launch_lean<T, 4, IdxT>(a, s);
+    // bf16 rows of 128 (4 per lane, 8 bytes): the lean kernel in exact mode,
+    // its replay for early stop / eps
+    const bool exact = a.max_iter < 0 && a.eps == 0.0f;
+    if (M == 128 && vec && exact && a.iters == nullptr && a.k <= lean::kListK) return launch_lean<T, 4, IdxT>(a, s);
+    if (M == 128 && vec && !exact && a.k <= lean::kListK) return launch_lean_replay<T, 4, IdxT>(a, s);
   }
   const int need = (M + GS - 1) / GS;
   const int G = need <= 4 ? need : (need <= 6 ? 6 : (need <= 8 ? 8 : (need <= 12 ? 12 : 16)));
