@@ -339,16 +339,18 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
       nm2 = P::midpoint(nlo2, nhi2);
       if (nm2 == nlo2 || nm2 == nhi2) break;  // no 16-bit value strictly inside
     }
-    uint32_t d[W];
     int acc = 0;
 #pragma unroll
-    for (int w = 0; w < W; ++w) d[w] = P::add(h[w], nm2);
-#pragma unroll
-    for (int w = 0; w + 1 < W; w += 2) acc = sum_bytes(half_signs(d[w], d[w + 1]), acc);
+    for (int w = 0; w + 1 < W; w += 2) acc = sum_bytes(half_signs(P::add(h[w], nm2), P::add(h[w + 1], nm2)), acc);
     const int tot = block_sum<TW>(acc, xc, par, lane, wib, bid);
     const float mv = -P::low_f32(nm2);  // the probe's value
     if (tot == kneg) {
-      // C(mid) == k: {h >= mid} is the top-k; this thread keeps NE + acc
+      // C(mid) == k: {h >= mid} is the top-k; this thread keeps NE + acc.
+      // The differences are formed again here rather than kept through the
+      // team barrier (16 fewer live registers across every pass).
+      uint32_t d[W];
+#pragma unroll
+      for (int w = 0; w < W; ++w) d[w] = P::add(h[w], nm2);
       if (!first && c_first != 0 && t_first != mv) {
         const float est = fabsf(float(c_first)) / fabsf(t_first - mv);
         rho = rho > 0.0f ? 0.8f * rho + 0.2f * est : est;
@@ -437,7 +439,9 @@ __device__ __forceinline__ void process_row_block(const uint32_t* __restrict__ s
 // list and exchange slots. Resident blocks per SM (registers; at most about
 // 70 KB of shared memory per block): 5 at 8 elements per thread, 3 at 16, 2 at
 // 32 (up to 128 registers, no spills; GB300, 2^16 rows: M = 2048 fp32 k = 64
-// 268 -> 191 us against 3 blocks, M = 8192 fp32 k = 256 1184 -> 955 us).
+// 268 -> 191 us against 3 blocks, M = 8192 fp32 k = 256 1184 -> 955 us; at 3
+// blocks the 80-register build spills 110-180 bytes, M = 4096 k = 256 387 ->
+// 564 us).
 template <typename T, int NE, int TW>
 struct LeanBlockCfg {
   static constexpr int RW = Lane<T, NE>::RW;
