@@ -502,7 +502,8 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
     api.rtopk_select(x, k, vals=vals, idx=idx)
     ev = vals[: 1 << 16].cpu().numpy()
     ei = idx[: 1 << 16].cpu().numpy()
-    for B in (2, 4, 8):
+    # B = 16 / 32 keep two / one elements per bucket (no search)
+    for B in (2, 4, 8, 16, 32):
         f = lambda: api.rtopk_select_bucketed(x, k, B, vals=vals, idx=idx)
         f()
         t_b = timed(f, reps) / reps * 1e3

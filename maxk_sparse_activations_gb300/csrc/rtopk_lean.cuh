@@ -828,6 +828,98 @@ __device__ __forceinline__ void process_row_bucketed(const uint32_t* __restrict_
   copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
 }
 
+// ---- one row split into B buckets that keep one or two elements each --------
+// Exact mode, k / B <= 2 (B = 2 .. 32 on a full row): no search. With
+// S = 32 / B lanes per bucket, each lane keeps its best one or two elements in
+// the definition's order (value descending, index ascending: only a strictly
+// larger value replaces, so among equal values the earlier index stays), then
+// log2(S) butterfly rounds merge the lanes' lists (a total order: indices are
+// distinct), and the first lane of each bucket writes the bucket's entries in
+// ascending index order straight to the CBSR row.
+template <typename T, int NE, int B, typename IdxT>
+__device__ __forceinline__ void process_row_bucket_small(const uint32_t* __restrict__ srow, int k, int lane,
+                                                         uint32_t* __restrict__ list, T* __restrict__ vrow,
+                                                         IdxT* __restrict__ irow, uint32_t& st) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int S = 32 / B;  // lanes per bucket
+  const int kb = k / B;      // 1 or 2
+  float x[NE];
+  reload<T, NE>(srow, lane, x);
+  float a = fabsf(x[0]);
+  int e = 1;
+#pragma unroll
+  for (; e + 1 < NE; e += 2) a = max3_nan(a, fabsf(x[e]), fabsf(x[e + 1]));
+  if (e < NE) a = max_nan(a, fabsf(x[e]));
+  if (!(warp_max_nan(a) <= 1e38f)) {
+    // invalid row: report which precondition fails, write the first k elements
+    bool nonfinite = false, range = false;
+#pragma unroll
+    for (int q = 0; q < NE; ++q) {
+      const float b = fabsf(x[q]);
+      nonfinite |= !(b <= 3.402823466e38f);
+      range |= (b > 1e38f && b <= 3.402823466e38f);
+    }
+    if (__any_sync(FULL, nonfinite)) st |= kStatusNonFinite;
+    if (__any_sync(FULL, range)) st |= kStatusRange;
+    for (int p = lane; p < k; p += 32) list[p] = uint32_t(p);
+    copy_out<T, Lane<T, NE>::RW, IdxT>(list, srow, k, lane, vrow, irow);
+    return;
+  }
+  // the lane's best two, in the definition's order
+  float v0 = x[0], v1 = neg_inf();
+  int i0 = lane * NE, i1 = -1;
+#pragma unroll
+  for (int q = 1; q < NE; ++q) {
+    const float xv = x[q];
+    const int j = lane * NE + q;
+    const bool g0 = xv > v0, g1 = xv > v1;
+    v1 = g0 ? v0 : (g1 ? xv : v1);
+    i1 = g0 ? i0 : (g1 ? j : i1);
+    v0 = g0 ? xv : v0;
+    i0 = g0 ? j : i0;
+  }
+  auto better = [](float av, int ai, float bv, int bi) { return av > bv || (av == bv && ai < bi); };
+#pragma unroll
+  for (int d = 1; d < S; d <<= 1) {
+    const float pv0 = __shfl_xor_sync(FULL, v0, d);
+    const int pi0 = __shfl_xor_sync(FULL, i0, d);
+    const bool mine = better(v0, i0, pv0, pi0);  // this lane's first is the merged first
+    if (kb == 2) {
+      const float pv1 = __shfl_xor_sync(FULL, v1, d);
+      const int pi1 = __shfl_xor_sync(FULL, i1, d);
+      // second: the better of (my second, partner's first) or (my first, partner's second)
+      const float av = mine ? v1 : v0, bv = mine ? pv0 : pv1;
+      const int ai = mine ? i1 : i0, bi = mine ? pi0 : pi1;
+      const bool ta = better(av, ai, bv, bi);
+      v1 = ta ? av : bv;
+      i1 = ta ? ai : bi;
+    }
+    v0 = mine ? v0 : pv0;
+    i0 = mine ? i0 : pi0;
+  }
+  auto bits = [](float v) -> T {
+    if constexpr (sizeof(T) == 4) {
+      return v;
+    } else {
+      return T(__float_as_uint(v) >> 16);  // the bf16 pattern the value was widened from
+    }
+  };
+  if ((lane & (S - 1)) == 0) {
+    const int b = lane / S;
+    if (kb == 1) {
+      vrow[b] = bits(v0);
+      irow[b] = IdxT(i0);
+    } else {
+      const bool o = i0 < i1;
+      vrow[2 * b] = bits(o ? v0 : v1);
+      irow[2 * b] = IdxT(o ? i0 : i1);
+      vrow[2 * b + 1] = bits(o ? v1 : v0);
+      irow[2 * b + 1] = IdxT(o ? i1 : i0);
+    }
+  }
+  __syncwarp();
+}
+
 // ---- one row, replay of the value-space bisection ---------------------------
 // Early stop (max_iter cap, eps) or exact mode with per-row pass counts: the
 // RTop-K summary page, "Approach": bisection over the row's value range
@@ -932,7 +1024,9 @@ constexpr bool kGuessRows = NE >= 32 || (NE >= 16 && sizeof(T) == 2);
 // (B > 1: B buckets per row, B dividing 32 and k). One warp per row,
 // persistent over rows; each warp keeps kStages rows in flight through
 // cp.async copies into its own shared stages.
-template <typename T, int NE, typename IdxT, int B = 1, bool GUESS = false>
+// SMALLB (B > 1): the buckets keep one or two elements each
+// (process_row_bucket_small) instead of searching side by side.
+template <typename T, int NE, typename IdxT, int B = 1, bool GUESS = false, bool SMALLB = false>
 __global__ void __launch_bounds__(256, LeanCfg<T, NE>::kBlocks)
 rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ vals, IdxT* __restrict__ idx,
                   uint32_t* __restrict__ status) {
@@ -968,6 +1062,8 @@ rtopk_lean_kernel(const T* __restrict__ in, int64_t N, int k, T* __restrict__ va
     __syncwarp();
     if constexpr (B == 1) {
       process_row<T, NE, IdxT, GUESS>(ring_all[wib][q], k, lane, list, vrow, irow, st, tprev, rho);
+    } else if constexpr (SMALLB) {
+      process_row_bucket_small<T, NE, B, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
     } else {
       process_row_bucketed<T, NE, B, IdxT>(ring_all[wib][q], k, lane, list, vrow, irow, st);
     }
