@@ -740,6 +740,22 @@ def _case_bucketed():
         api.rtopk_select_bucketed(x, 32, 4)
 
 
+def _case_spgemm():
+    # the MaxK-GNN forward aggregation of the bench extras: 2^17-node power-law
+    # graph (mean in-degree 64, capped at 4096), CBSR k = 32 of M = 256
+    import torch
+    from maxk_sparse_activations_gb300 import api, synth
+    dev = torch.device("cuda")
+    n, M, k = 1 << 17, 256, 32
+    row_ptr, col, w = synth.power_law_graph(n, n, 64.0, seed=5, alpha=2.5, max_degree=4096)
+    xb = torch.from_numpy(synth.normal_bf16(n, M, seed=0).view(np.int16)).view(torch.bfloat16).to(dev)
+    sd, si = api.maxk_forward(xb, k)
+    rp, cl, ww = (torch.from_numpy(a).to(dev) for a in (row_ptr, col, w))
+    out = torch.empty((n, M), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        api.maxk_spgemm_forward(rp, cl, ww, sd, si, M, out=out)
+
+
 def _case_long_rows():
     # exact rows of 4096 (the multi-warp 16-bit kernel, four warps per row):
     # 2^14 x 4096 fp32 N(0,1), k = 256 (268 MB in)
@@ -764,7 +780,7 @@ def _case_early_stop():
 
 PROFILE_CASES = {"cluster": _case_cluster, "fused-backward": _case_fused_backward, "early-stop": _case_early_stop,
                  "maxk-forward": _case_maxk_forward, "maxk-backward": _case_maxk_backward,
-                 "bucketed": _case_bucketed, "long-rows": _case_long_rows}
+                 "bucketed": _case_bucketed, "long-rows": _case_long_rows, "spgemm": _case_spgemm}
 
 
 def run_case(name: str) -> int:

@@ -38,12 +38,15 @@ constexpr uint32_t kStatusBadIndex = 0x8u;
 constexpr uint32_t kStatusBadEdge = 0x10u;
 constexpr int kThreads = 256;
 #ifndef RTOPK_SPMM_U
-#define RTOPK_SPMM_U 4
+#define RTOPK_SPMM_U 4  // k != 32 and the backward
 #endif
 #ifndef RTOPK_SPMM_HEAVY_WARPS
 #define RTOPK_SPMM_HEAVY_WARPS 8
 #endif
 constexpr int kU = RTOPK_SPMM_U;  // edges whose rows are in flight together
+// the same for the k == 32 loop (GB300, 2^17-node power-law graph: 576 /
+// 497 / 582 us at 4 / 8 / 16)
+constexpr int kU32 = 8;
 constexpr int kHeavyThreads = 32 * RTOPK_SPMM_HEAVY_WARPS;  // warps sharing one heavy row
 // Rows with more edges than this are split over the warps of one block.
 constexpr int64_t kHeavyEdges = 512;
@@ -105,6 +108,102 @@ __device__ __forceinline__ void accumulate_edges(float* __restrict__ acc, const 
   }
 }
 
+// k == 32 (one CBSR entry per lane, the MaxK layer's shape): the same sums in
+// the same order with no per-lane branch. A batch of 32 edges is validated
+// once (a ballot of bad source rows; an edge is skipped with a warp-uniform
+// test), the entries of U edges are loaded unconditionally (a skipped edge
+// reads row 0, which exists because n_src > 0 is checked first), offsets are
+// 32-bit when n_src * k fits, and a column index outside [0, M) is added into
+// the accumulator's spare slot M instead of branching (and flagged). A full
+// batch of valid edges (nearly all) runs without per-edge tests. GB300,
+// 2^17-node power-law graph (8.05 M edges), M = 256: the forward (with the
+// heavy rows) 1208 -> 497 us.
+__device__ __forceinline__ void accumulate_edges_k32(float* __restrict__ acc, const int32_t* __restrict__ col,
+                                                     const float* __restrict__ w, int64_t e0, int64_t e1,
+                                                     int64_t n_src, const uint16_t* __restrict__ sp_data,
+                                                     const int16_t* __restrict__ sp_index, int M, int lane,
+                                                     uint32_t& st) {
+  if (n_src <= 0) {
+    if (e1 > e0) st |= kStatusBadEdge;
+    return;
+  }
+  const bool off32 = n_src * 32 <= int64_t(0x7fffffff);
+  bool bad_index = false;
+  for (int64_t c0 = e0; c0 < e1; c0 += 32) {
+    const int nc = (e1 - c0 < 32) ? int(e1 - c0) : 32;
+    const int32_t cj = (lane < nc) ? col[c0 + lane] : 0;
+    const float cw = (lane < nc) ? (w != nullptr ? w[c0 + lane] : 1.0f) : 0.0f;
+    const bool bad_lane = lane < nc && !(cj >= 0 && cj < n_src);
+    const unsigned bad = __ballot_sync(0xffffffffu, bad_lane);
+    if (bad != 0u) st |= kStatusBadEdge;
+    const int32_t cjs = bad_lane ? 0 : cj;  // a row that exists
+    if (nc == 32 && bad == 0u) {
+      // a full batch of valid edges (almost every batch): no per-edge tests
+#pragma unroll 1
+      for (int u = 0; u < 32; u += kU32) {
+        uint16_t dv[kU32];
+        int16_t di[kU32];
+        float we[kU32];
+#pragma unroll
+        for (int q = 0; q < kU32; ++q) {
+          const int32_t j = __shfl_sync(0xffffffffu, cjs, u + q);
+          we[q] = __shfl_sync(0xffffffffu, cw, u + q);
+          if (off32) {
+            const uint32_t o = uint32_t(j) * 32u + uint32_t(lane);
+            dv[q] = sp_data[o];
+            di[q] = sp_index[o];
+          } else {
+            const int64_t o = int64_t(j) * 32 + lane;
+            dv[q] = sp_data[o];
+            di[q] = sp_index[o];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kU32; ++q) {
+          const uint32_t m = uint32_t(int32_t(di[q]));
+          const bool in = m < uint32_t(M);
+          bad_index |= !in;
+          const uint32_t slot = in ? m : uint32_t(M);
+          acc[slot] = __fadd_rn(acc[slot], __fmul_rn(we[q], bf16f(dv[q])));
+          __syncwarp();
+        }
+      }
+      continue;
+    }
+    for (int u = 0; u < nc; u += kU32) {
+      uint16_t dv[kU32];
+      int16_t di[kU32];
+      float we[kU32];
+#pragma unroll
+      for (int q = 0; q < kU32; ++q) {
+        const int32_t j = __shfl_sync(0xffffffffu, cjs, (u + q) & 31);
+        we[q] = __shfl_sync(0xffffffffu, cw, (u + q) & 31);
+        if (off32) {
+          const uint32_t o = uint32_t(j) * 32u + uint32_t(lane);
+          dv[q] = sp_data[o];
+          di[q] = sp_index[o];
+        } else {
+          const int64_t o = int64_t(j) * 32 + lane;
+          dv[q] = sp_data[o];
+          di[q] = sp_index[o];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kU32; ++q) {
+        if (u + q < nc && !((bad >> ((u + q) & 31)) & 1u)) {  // warp-uniform
+          const uint32_t m = uint32_t(int32_t(di[q]));
+          const bool in = m < uint32_t(M);
+          bad_index |= !in;
+          const uint32_t slot = in ? m : uint32_t(M);
+          acc[slot] = __fadd_rn(acc[slot], __fmul_rn(we[q], bf16f(dv[q])));
+          __syncwarp();
+        }
+      }
+    }
+  }
+  if (bad_index) st |= kStatusBadIndex;
+}
+
 __device__ __forceinline__ void zero_row(float* __restrict__ acc, int M, int lane, bool vec) {
   if (vec) {
     for (int m = lane * 4; m < M; m += 128) *reinterpret_cast<float4*>(acc + m) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -113,7 +212,9 @@ __device__ __forceinline__ void zero_row(float* __restrict__ acc, int M, int lan
   }
 }
 
-// Destination rows with at most `heavy` edges: one warp per row, edges in order.
+// Destination rows with at most `heavy` edges: one warp per row, edges in
+// order, rows round-robin over the warps (contiguous row ranges with equal
+// edge counts per warp measured no faster on a power-law graph).
 template <int KS>
 __global__ void __launch_bounds__(kThreads)
 spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
@@ -124,7 +225,7 @@ spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
-  float* acc = acc_all + size_t(wib) * M;
+  float* acc = acc_all + size_t(wib) * (M + 4);  // M columns + a spare slot, 16-byte aligned
   const int64_t nw = int64_t(gridDim.x) * wpb;
   uint32_t st = 0;
   for (int64_t i = int64_t(blockIdx.x) * wpb + wib; i < n_dst; i += nw) {
@@ -132,7 +233,11 @@ spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict
     if (e1 - e0 > heavy) continue;  // left to spgemm_heavy_kernel
     zero_row(acc, M, lane, vec);
     __syncwarp();
-    accumulate_edges<KS>(acc, col, w, e0, e1, n_src, sp_data, sp_index, M, k, lane, st);
+    if (KS == 1 && k == 32) {
+      accumulate_edges_k32(acc, col, w, e0, e1, n_src, sp_data, sp_index, M, lane, st);
+    } else {
+      accumulate_edges<KS>(acc, col, w, e0, e1, n_src, sp_data, sp_index, M, k, lane, st);
+    }
     float* o = out + i * int64_t(M);
     if (vec) {
       for (int m = lane * 4; m < M; m += 128) __stcs(reinterpret_cast<float4*>(o + m), *reinterpret_cast<const float4*>(acc + m));
@@ -145,9 +250,11 @@ spgemm_fwd_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restrict
 }
 
 // Destination rows with more than `heavy` edges: one block (up to
-// kHeavyThreads / 32 warps) per row. Warp q adds the edge chunks q, q + W, ... (chunks of `heavy` edges,
-// each in edge order) into its own accumulator; the W partial rows are then
-// summed in warp order. Deterministic, but the terms of such a row are not added in plain
+// kHeavyThreads / 32 warps) per row. The row's edges are cut into W equal
+// chunks (multiples of 32 edges); warp q adds chunk q, in edge order, into its
+// own accumulator, and the W partial rows are then summed in warp order
+// (fixed 512-edge chunks left most warps of a 600-edge row waiting at the
+// barrier). Deterministic, but the terms of such a row are not added in plain
 // edge order (the bound on the difference is in the C ABI header).
 template <int KS>
 __global__ void __launch_bounds__(kHeavyThreads)
@@ -159,7 +266,7 @@ spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restri
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
-  float* acc = acc_all + size_t(wib) * M;
+  float* acc = acc_all + size_t(wib) * (M + 4);  // M columns + a spare slot, 16-byte aligned
   uint32_t st = 0;
   // every warp reads the same 32 row lengths, so the ballot is block-uniform
   for (int64_t i0 = int64_t(blockIdx.x) * 32; i0 < n_dst; i0 += int64_t(gridDim.x) * 32) {
@@ -172,15 +279,24 @@ spgemm_heavy_kernel(const int64_t* __restrict__ row_ptr, const int32_t* __restri
     const int64_t e0 = row_ptr[i], e1 = row_ptr[i + 1];
     zero_row(acc, M, lane, vec);
     __syncwarp();
-    for (int64_t c0 = e0 + int64_t(wib) * heavy; c0 < e1; c0 += int64_t(wpb) * heavy) {
-      const int64_t c1 = (e1 - c0 < heavy) ? e1 : c0 + heavy;
-      accumulate_edges<KS>(acc, col, w, c0, c1, n_src, sp_data, sp_index, M, k, lane, st);
+    // the row's edges in wpb equal chunks (multiples of 32 edges): warp q adds
+    // chunk q in edge order
+    int64_t chunk = (e1 - e0 + wpb - 1) / wpb;
+    chunk = (chunk + 31) & ~int64_t(31);
+    const int64_t c0 = e0 + int64_t(wib) * chunk;
+    const int64_t c1 = (e1 - c0 < chunk) ? e1 : c0 + chunk;
+    if (c0 < c1) {
+      if (KS == 1 && k == 32) {
+        accumulate_edges_k32(acc, col, w, c0, c1, n_src, sp_data, sp_index, M, lane, st);
+      } else {
+        accumulate_edges<KS>(acc, col, w, c0, c1, n_src, sp_data, sp_index, M, k, lane, st);
+      }
     }
     __syncthreads();
     float* o = out + i * int64_t(M);
     for (int m = threadIdx.x; m < M; m += blockDim.x) {
       float sum = acc_all[m];
-      for (int q = 1; q < wpb; ++q) sum = __fadd_rn(sum, acc_all[size_t(q) * M + m]);
+      for (int q = 1; q < wpb; ++q) sum = __fadd_rn(sum, acc_all[size_t(q) * (M + 4) + m]);
       __stcs(o + m, sum);
     }
     __syncthreads();
@@ -293,13 +409,18 @@ cudaError_t launch_rows(Kern kern, int64_t rows, size_t smem_per_warp, cudaStrea
 }
 
 // Heavy rows: as many warps per block as the 48 KB of shared accumulators allow
-// (up to kHeavyThreads / 32), one block per heavy row.
+// (up to kHeavyThreads / 32), one block per group of 32 rows.
 template <typename Kern>
 cudaError_t launch_heavy(Kern kern, int64_t rows, size_t smem_per_warp, int& threads, int& blocks) {
   int wpb = int((48 * 1024) / smem_per_warp);
   wpb = wpb > kHeavyThreads / 32 ? kHeavyThreads / 32 : (wpb < 1 ? 1 : wpb);
   threads = wpb * 32;
-  blocks = persistent_blocks(reinterpret_cast<const void*>(kern), threads, smem_per_warp * wpb, rows);
+  // one block per 32-row group: a block meets only its group's heavy rows, so
+  // the heavy rows of the graph spread over the SMs instead of queueing in a
+  // persistent block; blocks of groups without one exit at once (2^17-node
+  // power-law graph, 1118 rows > 512 edges: the forward 1207 -> 923 us)
+  blocks = rows > 0x7fffffff ? 0x7fffffff : int(rows);
+  (void)kern;
   return blocks > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
@@ -309,7 +430,7 @@ cudaError_t launch_spgemm_fwd(const int64_t* row_ptr, const int32_t* col, const 
                               int64_t n_src, const uint16_t* sp_data, const int16_t* sp_index, int M, int k,
                               float* out, uint32_t* status, cudaStream_t s) {
   const int ks = (k + 31) / 32;
-  const size_t smem_warp = size_t(M) * sizeof(float);
+  const size_t smem_warp = size_t(M + 4) * sizeof(float);  // M columns + a spare slot, 16-byte aligned
   // 16-byte accumulator and output rows need M % 4 == 0 and an aligned output
   const bool vec = (M % 4 == 0) && ((reinterpret_cast<uintptr_t>(out) & 15u) == 0);
   int threads = 0, blocks = 0;
