@@ -29,6 +29,7 @@
 
 #include "rtopk_block.cuh"
 
+
 namespace rtopk {
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -146,6 +147,7 @@ rtopk_cluster_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_
     }
   };
   float x[G][V];
+  float tprev = __int_as_float(0x7fc00000);  // the cluster's previous threshold (guessed probes)
   for (int64_t r = cluster_index(); r < N; r += cluster_count()) {
     load(r, x);
 
@@ -214,7 +216,68 @@ rtopk_cluster_kernel(const T* __restrict__ in, int64_t N, int M, int k, int max_
         return V == 8 && bf16_stop && __fsub_rn(hi, lo) <= fmaxf(fabsf(lo), fabsf(hi)) * 0.015625f + 1e-38f &&
                bf16_single_value(lo, hi);
       };
+      // Exact mode without pass counts: the round's middle probe is a guess --
+      // the cluster's previous threshold in the first round, then the point
+      // where the count, interpolated linearly between the bracket ends'
+      // counts, crosses k + 1/2 -- and the outer probes the midpoints of the
+      // two sub-brackets, so a poor guess still halves the bracket. Any count
+      // of exactly k ends the search with the exact fill; the set is the same
+      // whatever probes are taken. fp32 rows only: GB300, fp32 N(0,1), k = 64
+      // / 256 / 1024: M = 16384 863 / 926 / 1070 -> 826 / 843 / 928 us, M =
+      // 65536 850 / 910 / 978 -> 833 / 853 / 844 us; bf16 rows (ties at the
+      // k-th value end on the single-value test anyway) were 1-3% slower.
+      if (EXACT && iters == nullptr && V == 4) {
+        int c_lo = M, c_hi = int(team_sum<C>(sh, buf ^ 1, 0, lane, TW));  // C(hi) from the max-tie round
+        bool first = true;
+        for (;;) {
+          if (it >= kSafetyCap) {
+            st |= kStatusSafetyCap;
+            break;
+          }
+          const float mid = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
+          if (!(lo < mid && mid < hi)) break;  // no binary32 value strictly inside
+          float g = first ? tprev
+                          : fmaf(hi - lo, (float(c_lo - k) - 0.5f) / float(c_lo - c_hi), lo);
+          first = false;
+          const float m1 = (lo < g && g < hi) ? g : mid;
+          const float mL = __fmul_rn(__fadd_rn(lo, m1), 0.5f);
+          const float mR = __fmul_rn(__fadd_rn(m1, hi), 0.5f);
+          unsigned l1, lL, lR;
+          lane_count_lt3<G, V>(x, m1, mL, mR, l1, lL, lR);
+          cluster_round<C, 3>(sh, buf, t, lane, unsigned(32 * NE) - __reduce_add_sync(0xffffffffu, l1),
+                              unsigned(32 * NE) - __reduce_add_sync(0xffffffffu, lL),
+                              unsigned(32 * NE) - __reduce_add_sync(0xffffffffu, lR));
+          const int c1 = int(team_sum<C>(sh, buf, 0, lane, TW));
+          const int cL = int(team_sum<C>(sh, buf, 1, lane, TW));
+          const int cR = int(team_sum<C>(sh, buf, 2, lane, TW));
+          last = buf;
+          buf ^= 1;
+          ++it;
+          // counts are non-increasing in the threshold: mL <= m1 <= mR
+          if (cL == k || c1 == k || cR == k) {
+            lastw = cL == k ? 1 : (c1 == k ? 0 : 2);
+            lo = cL == k ? mL : (c1 == k ? m1 : mR);
+            eq = true;
+            break;
+          }
+          if (cR > k) {
+            lo = mR; c_lo = cR;
+          } else if (c1 > k) {
+            lo = m1; c_lo = c1; hi = mR; c_hi = cR;
+          } else if (cL > k) {
+            lo = mL; c_lo = cL; hi = m1; c_hi = c1;
+          } else {
+            hi = mL; c_hi = cL;
+          }
+          // one bf16 value left in [lo, hi): the kept set is final
+          if (V == 8 && __fsub_rn(hi, lo) <= fmaxf(fabsf(lo), fabsf(hi)) * 0.015625f + 1e-38f &&
+              bf16_single_value(lo, hi))
+            break;
+        }
+        if (eq) tprev = lo;
+      }
       for (;;) {
+        if (EXACT && iters == nullptr && V == 4) break;  // searched above
         if (stop_before_pass()) break;
         const float m1 = __fmul_rn(__fadd_rn(lo, hi), 0.5f);
         if (!(lo < m1 && m1 < hi)) break;
