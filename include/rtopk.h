@@ -117,11 +117,14 @@ int rtopk_select(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_it
  *
  *  iters   device, N int32 or NULL: counted bisection passes of each row
  *  status  device, one uint32 or NULL: OR of RTOPK_STATUS_* bits over all rows
- * Performance note: with iters != NULL every row runs the binary32 search whose
- * passes are counted. In exact mode with iters == NULL (and in rtopk_select /
- * maxk_forward) rows of 128..512 elements may instead run a search counted on
- * packed 16-bit images of the row, finished in binary32 where needed: same
- * outputs, fewer instructions.
+ * Performance note: with iters != NULL in exact mode every row runs the
+ * binary32 search whose passes are counted. In exact mode with iters == NULL
+ * (and in rtopk_select / maxk_forward) rows of 128..1024 elements (one warp per
+ * row) and of 2048 / 4096 / 8192 elements (a team of warps per row) may
+ * instead run a search counted on packed 16-bit images of the row, finished in
+ * binary32 where needed: same outputs, fewer instructions. Early stop and eps
+ * on rows of 128..1024 follow the same binary32 trajectory on a kernel that
+ * streams rows through shared memory.
  */
 int rtopk_select_stats(const void* in, int64_t N, int32_t M, int32_t k, int32_t max_iter,
                        float eps, int32_t dtype, void* vals, int32_t* idx, int32_t* iters,
@@ -183,8 +186,9 @@ int maxk_backward_scatter(const void* dy_bf16, const int16_t* idx, int64_t N, in
  *              col_idx[e]; binary32 products and sums, one rounding each, no
  *              FMA -- deterministic, and bit-identical to that sequential sum
  *              for rows of at most 512 edges. Longer rows are split into
- *              chunks of 512 edges summed by the warps of one block and then
- *              combined in a fixed order: still deterministic, and within
+ *              equal chunks (multiples of 32 edges), one per warp of a block,
+ *              each summed in edge order, and the partial rows are combined
+ *              in warp order: still deterministic, and within
  *              2 (deg + 1) 2^-24 sum|terms| of the sequential sum.
  *
  *  row_ptr      device, n_dst + 1 int64: CSR offsets over destination rows

@@ -1,4 +1,4 @@
-"""GPU parity of exact mode without pass counts on rows of 128..512 elements.
+"""GPU parity of exact mode without pass counts on rows of 128..1024 elements.
 
 There the kernel runs its threshold search on packed 16-bit images of the row
 (binary16 for fp32 rows, the data themselves for bf16 rows) and finishes in
