@@ -473,7 +473,7 @@ def secondary_measurements(torch, api, synth, dev, x, stream, world, timed):
     vals = torch.empty((N, k), dtype=torch.float32, device=dev)
     idx = torch.empty((N, k), dtype=torch.int32, device=dev)
     reps = 50
-    for m in (-1, 2, 5):
+    for m in (-1, 2, 3, 4, 5, 8):  # the early-stop settings of the MaxK-shaped configuration
         f = lambda: api.rtopk_select(x, k, m, 0.0, vals=vals, idx=idx)
         f()
         out[f"rtopk_f32_max_iter_{m}_us"] = timed(f, reps) / reps * 1e3

@@ -519,3 +519,29 @@ def test_long_rows_saturated_images(M, case):
         torch.cuda.synchronize()
         ov, oi = oracle.sort_topk(x, k)
         assert_same_selection(v, i, ov, oi, what=f"saturated {case} M={M} k={k}")
+
+
+@pytest.mark.parametrize("M,dtype", [(1024, "f32"), (512, "bf16"), (1024, "bf16"), (2048, "f32"), (4096, "bf16"),
+                                     (8192, "f32"), (16384, "f32")])
+def test_guessed_probes_under_shifting_row_scales(M, dtype):
+    """Exact mode without pass counts probes guessed thresholds (the previous
+    row's, then Newton or interpolation steps with a density carried over
+    rows). Consecutive rows here differ in scale by up to 10^6 and in sign, so
+    the carried guesses and densities are wrong by orders of magnitude: every
+    row must still be the definition (a guess only ever replaces a midpoint
+    strictly inside the bracket)."""
+    N = 203
+    g = np.random.default_rng(M + 17)
+    base = g.standard_normal((N, M)).astype(np.float32)
+    scale = np.array([1e-3, 1.0, 1e3, -1.0, 3e-3, -1e3, 0.5], dtype=np.float32)[np.arange(N) % 7]
+    x = base * scale[:, None]
+    if dtype == "bf16":
+        x = synth.f32_to_bf16_bits(x)
+    xt = to_dev(x)
+    for k in (33, 64, 256, 1000):
+        if k > M:
+            continue
+        v, i = api.rtopk_select(xt, k)
+        torch.cuda.synchronize()
+        ov, oi = oracle.sort_topk(x, k)
+        assert_same_selection(v, i, ov, oi, what=f"shifting scales M={M} {dtype} k={k}")
