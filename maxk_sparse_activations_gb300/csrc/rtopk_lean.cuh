@@ -925,11 +925,12 @@ __device__ __forceinline__ void process_row_bucket_small(const uint32_t* __restr
 // the lane's classification as two bit masks from the sign bits of x - hi and
 // x - lo (set: x below the end), lane counts by popc, one warp scan of both
 // counts, and the lane's kept elements stored by walking its kept-bit mask.
-// Used from 16 elements per lane (GB300, k = 32: rows of 1024 at max_iter 2 /
-// 5: fp32 305 / 370 -> 270 / 315 us, bf16 308 / 370 -> 246 / 293 us; rows of
-// 512 at max_iter 5 7-8% faster, at 2 within 2%); with 4-12 elements per lane
-// the divergent mask walk costs more than one predicated store per element
-// (rows of 128 at max_iter 2: 271 -> 347 us).
+// Used at 32 elements per lane with k <= 32 (GB300, rows of 1024, max_iter 2:
+// fp32 k = 16 / 32 306 / 308 -> 277 / 285 us, bf16 304 / 310 -> 261 / 269 us;
+// max_iter 5, k = 32: fp32 370 -> 315 us). Where a lane keeps many elements
+// (k >= 64: rows of 512, k = 256: 195 -> 230 us) or holds fewer (rows of 512,
+// k = 32: 160 -> 173 us; rows of 128: 271 -> 347 us) the divergent mask walk
+// costs more than one predicated store per element.
 template <int NE>
 __device__ __forceinline__ void stage_general_masks(const float (&x)[NE], float lo, float hi, int k, int lane,
                                                     uint32_t* __restrict__ list) {
@@ -1041,7 +1042,9 @@ __device__ __forceinline__ void process_row_replay(const uint32_t* __restrict__ 
         if (cnt == k) break;
       }
     }
-    if constexpr (NE >= 16) {
+    bool masks = false;
+    if constexpr (NE >= 32) masks = k <= 32;
+    if (masks) {
       stage_general_masks<NE>(x, lo, hi, k, lane, list);
     } else {
       stage_general<NE>(x, lo, hi, k, lane, list);
