@@ -545,3 +545,21 @@ def test_guessed_probes_under_shifting_row_scales(M, dtype):
         torch.cuda.synchronize()
         ov, oi = oracle.sort_topk(x, k)
         assert_same_selection(v, i, ov, oi, what=f"shifting scales M={M} {dtype} k={k}")
+
+
+@pytest.mark.parametrize("M", [128, 256, 512, 1024, 2048, 3000])
+@pytest.mark.parametrize("value_set", ["normal", "int_ties", "signed_zeros"])
+def test_maxk_forward_early_stop_and_eps(M, value_set):
+    """maxk_forward (bf16 in, int16 indices) with early stop and eps follows the
+    pages' trajectory like rtopk_select: every row against the oracle's replay
+    (the replay kernel on full rows of 128..1024, the binary32 kernels
+    elsewhere), values and indices."""
+    N = 777
+    x = synth.make(value_set, N, M, seed=M + 29, dtype="bf16")
+    xt = to_dev(x)
+    for k in (1, 32, min(M, 200)):
+        for m, eps in ((0, 0.0), (2, 0.0), (5, 0.0), (-1, 1e-2), (3, 1e-3)):
+            fv, fi = api.maxk_forward(xt, k, m, eps)
+            torch.cuda.synchronize()
+            ov, oi, _ = oracle.replay(x, k, m, eps)
+            assert_same_selection(fv, fi, ov, oi, what=f"maxk_forward {value_set} M={M} k={k} max_iter={m} eps={eps}")
